@@ -1,0 +1,36 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built CUDA library")
+
+
+def read_golden(name):
+    """Parse a golden fixture: 'bytes', 'values' and 'at <index> <value>' lines."""
+    blocks, cur = [], None
+    with open(os.path.join(GOLDEN, name)) as f:
+        for raw in f:
+            line = raw.split("#", 1)[0].strip()
+            if not line:
+                continue
+            key, rest = line.split(None, 1)
+            if key == "bytes":
+                cur = {"bytes": bytes.fromhex(rest), "values": None, "at": {}}
+                blocks.append(cur)
+            elif key == "values":
+                cur["values"] = [float(v) for v in rest.split()]
+            elif key == "at":
+                idx, val = rest.split()
+                cur["at"][int(idx)] = float(val)
+            else:
+                blocks.append((int(key), float(rest)))
+    return blocks

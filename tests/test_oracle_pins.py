@@ -1,0 +1,316 @@
+"""Pins of the CPU oracle to values fixed outside it (no GPU needed).
+
+Each check would fail on a plausible mistake in the oracle: a wrong field
+offset or nibble order (hand-derived golden blocks), a dropped sign (negative
+scales), a wrong exponent bias or subnormal rule (exhaustive code tables
+against numpy / torch), a dropped or extra term or a transposed operand in the
+product (one-hot permutation, exact integer matmul, library matmul).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from conftest import read_golden
+
+
+def _same(a, b):
+    """Equal values with the same sign of zero, or both NaN."""
+    if math.isnan(a) or math.isnan(b):
+        return math.isnan(a) and math.isnan(b)
+    return a == b and math.copysign(1, a) == math.copysign(1, b)
+
+
+# ---- scalar codes ------------------------------------------------------------
+
+def test_fp16_all_codes_match_numpy():
+    codes = np.arange(65536, dtype=np.uint16)
+    got = oracle.fp16(codes)
+    want = codes.view(np.float16).astype(np.float64)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
+
+
+def test_fp16_subnormal_and_specials():
+    # exponent field 0 is mantissa * 2^-24 (hrx-rs patch_bench.rs, fn float)
+    assert oracle.fp16([0x0001])[0] == 2.0 ** -24
+    assert oracle.fp16([0x03FF])[0] == 1023 * 2.0 ** -24
+    assert oracle.fp16([0x7BFF])[0] == 65504.0
+    assert oracle.fp16([0xFC00])[0] == -math.inf
+
+
+def test_e4m3_all_codes_match_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.e4m3(codes)
+    want = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    for c in range(256):
+        assert _same(got[c], want[c]), (c, got[c], want[c])
+
+
+def test_e4m3_scale_bytes_of_the_moe_workload():
+    # (r & 7) | 0x38 gives 1.0, 1.125, ..., 1.875 (memra synth_rows)
+    got = oracle.e4m3([0x38 | r for r in range(8)])
+    assert list(got) == [1.0 + r / 8 for r in range(8)]
+
+
+def test_e2m1_all_codes_match_ocp_table():
+    table = read_golden("e2m1_ocp.txt")
+    assert len(table) == 16
+    got = oracle.e2m1([c for c, _ in table])
+    for (c, v), g in zip(table, got):
+        assert _same(g, v), (c, g, v)
+
+
+# ---- block decoders ----------------------------------------------------------
+
+@pytest.mark.parametrize("fname,fmt", [("q4_0_blocks.txt", "q4_0"), ("q8_0_blocks.txt", "q8_0")])
+def test_whole_blocks_match_hand_values(fname, fmt):
+    blocks = read_golden(fname)
+    assert blocks
+    for blk in blocks:
+        got = oracle.decode(fmt, np.frombuffer(blk["bytes"], np.uint8), 1, 32)[0]
+        for e, (g, w) in enumerate(zip(got, blk["values"])):
+            assert _same(g, w), (fname, e, g, w)
+
+
+@pytest.mark.parametrize("fname,fmt,k", [("q4_k_block.txt", "q4_k", 256), ("q6_k_block.txt", "q6_k", 256),
+                                         ("nvfp4_group.txt", "nvfp4", 64)])
+def test_block_spot_values_match_hand_values(fname, fmt, k):
+    (blk,) = read_golden(fname)
+    assert len(blk["bytes"]) == oracle.block_bytes(fmt)
+    got = oracle.decode(fmt, np.frombuffer(blk["bytes"], np.uint8), 1, k)[0]
+    assert len(blk["at"]) >= 8
+    for e, w in blk["at"].items():
+        assert got[e] == w, (fname, e, got[e], w)
+
+
+def _pack_q4k_scales(sc, mn):
+    """Independent packer for the 12 Q4_K scale bytes (the inverse direction of
+    the oracle's unpacking, written bit field by bit field)."""
+    out = [0] * 12
+    for j in range(4):
+        out[j] = (sc[j] & 63) | ((sc[j + 4] >> 4) << 6)
+        out[j + 4] = (mn[j] & 63) | ((mn[j + 4] >> 4) << 6)
+        out[j + 8] = (sc[j + 4] & 15) | ((mn[j + 4] & 15) << 4)
+    return out
+
+
+def test_q4k_every_scale_and_min_round_trips():
+    # For each sub-block and each 6-bit value, a block whose nibbles are all 1
+    # and d = 1, dmin = 0 decodes to the sub-block's scale; with nibbles 0 and
+    # dmin = -1 it decodes to its min.  Other sub-blocks get a different value.
+    rng = np.random.default_rng(7)
+    for trial in range(64):
+        sc = list(rng.integers(0, 64, 8))
+        mn = list(rng.integers(0, 64, 8))
+        scales = _pack_q4k_scales(sc, mn)
+        ones = bytes([0x00, 0x3C, 0x00, 0x00] + scales + [0x11] * 128)
+        got = oracle.decode("q4_k", np.frombuffer(ones, np.uint8), 1, 256)[0]
+        for j in range(8):
+            assert np.all(got[32 * j:32 * j + 32] == sc[j]), (trial, j)
+        zeros = bytes([0x00, 0x3C, 0x00, 0xBC] + scales + [0x00] * 128)
+        got = oracle.decode("q4_k", np.frombuffer(zeros, np.uint8), 1, 256)[0]
+        for j in range(8):
+            assert np.all(got[32 * j:32 * j + 32] == mn[j]), (trial, j)
+
+
+def test_q4k_nibble_positions():
+    # A single nonzero nibble anywhere lands on exactly one element: byte i of
+    # the nibble area feeds element 64*(i//32) + i%32 (low) and +32 (high).
+    for i in range(128):
+        for high in (0, 1):
+            qs = [0] * 128
+            qs[i] = 0x50 if high else 0x05
+            sc = _pack_q4k_scales([1] * 8, [0] * 8)
+            b = bytes([0x00, 0x3C, 0x00, 0x00] + sc + qs)
+            got = oracle.decode("q4_k", np.frombuffer(b, np.uint8), 1, 256)[0]
+            e = 64 * (i // 32) + i % 32 + 32 * high
+            want = np.zeros(256)
+            want[e] = 5.0
+            assert np.array_equal(got, want), (i, high)
+
+
+def test_q6k_bit_positions():
+    # Setting one low nibble or one high 2-bit pair moves exactly one element
+    # away from -32 (all-zero codes, scales 1, d = 1).
+    base_ql, base_qh = [0] * 128, [0] * 64
+    sc = [1] * 16
+
+    def decode(ql, qh):
+        b = bytes(ql + qh + sc + [0x00, 0x3C])
+        return oracle.decode("q6_k", np.frombuffer(b, np.uint8), 1, 256)[0]
+
+    for i in range(128):
+        for hi_nib in (0, 1):
+            ql = list(base_ql)
+            ql[i] = 0x30 if hi_nib else 0x03
+            got = decode(ql, base_qh)
+            h, rem = divmod(i, 64)
+            s = (rem >= 32) + 2 * hi_nib
+            e = 128 * h + 32 * s + rem % 32
+            want = np.full(256, -32.0)
+            want[e] = -29.0
+            assert np.array_equal(got, want), (i, hi_nib)
+    for i in range(64):
+        for s in range(4):
+            qh = list(base_qh)
+            qh[i] = 1 << (2 * s)
+            got = decode(base_ql, qh)
+            h, l = divmod(i, 32)
+            e = 128 * h + 32 * s + l
+            want = np.full(256, -32.0)
+            want[e] = -16.0
+            assert np.array_equal(got, want), (i, s)
+
+
+def test_q6k_scale_index_and_sign():
+    # Scale number i covers the 16 elements the reading assigns to it.
+    for i in range(16):
+        sc = [0] * 16
+        sc[i] = -2
+        b = bytes([0] * 128 + [0] * 64 + [s & 0xFF for s in sc] + [0x00, 0x3C])
+        got = oracle.decode("q6_k", np.frombuffer(b, np.uint8), 1, 256)[0]
+        h, rest = divmod(i, 8)
+        s, half = divmod(rest, 2)
+        idx = [128 * h + 32 * s + 16 * half + t for t in range(16)]
+        want = np.zeros(256)
+        want[idx] = 64.0  # -2 * (0 - 32)
+        assert np.array_equal(np.abs(got), np.abs(want)), i
+        assert np.all(got[idx] == 64.0)
+
+
+def test_nvfp4_every_code_and_scale_slot():
+    for slot in range(4):
+        for code in range(16):
+            scales = [0x38] * 4
+            scales[slot] = 0x3F  # 1.875
+            nib = bytes([code | (code << 4)] * 32)
+            got = oracle.decode("nvfp4", np.frombuffer(bytes(scales) + nib, np.uint8), 1, 64)[0]
+            e2m1 = oracle.e2m1([code])[0]
+            want = np.full(64, e2m1)
+            want[16 * slot:16 * slot + 16] *= 1.875
+            assert np.array_equal(got, want)
+
+
+def test_row_bytes_match_the_packed_sizes():
+    # cera VARIANTS src0_bytes and memra synth_rows (in_f/64 * 36)
+    assert oracle.row_bytes("f32", 1024) == 4096
+    assert oracle.row_bytes("q4_0", 1024) == 1024 // 32 * 18
+    assert oracle.row_bytes("q8_0", 4608) == 4608 // 32 * 34
+    assert oracle.row_bytes("q4_k", 4608) == 4608 // 256 * 144
+    assert oracle.row_bytes("q6_k", 1024) == 840
+    assert oracle.row_bytes("nvfp4", 4096) == 2304
+    assert oracle.row_bytes("q4_k", 1000) == 0
+
+
+# ---- dequant -----------------------------------------------------------------
+
+def test_dequant_is_the_decoded_value_rounded_once():
+    import synth
+    for fmt, k in [("q4_0", 64), ("q8_0", 64), ("q4_k", 256), ("q6_k", 256), ("nvfp4", 128)]:
+        m = 8
+        w = synth.weights(fmt, m, k, m * oracle.row_bytes(fmt, k))
+        exact = oracle.decode(fmt, w, m, k)
+        got = oracle.dequant(fmt, w, m, k)
+        assert np.array_equal(got, exact.astype(np.float32)), fmt
+        # decoded values are exact in f32 except Q4_K's d*sc*q - dmin*min,
+        # a difference of two products that can need more than 24 bits
+        if fmt != "q4_k":
+            assert np.array_equal(got.astype(np.float64), exact), fmt
+    w = synth.weights("nvfp4", 2, 64, 72)
+    got = oracle.dequant("nvfp4", w, 2, 64, tensor_scale=0.3)
+    want = (oracle.decode("nvfp4", w, 2, 64) * float(np.float32(0.3))).astype(np.float32)
+    assert np.array_equal(got, want)
+
+
+# ---- the product -------------------------------------------------------------
+
+def _q8_0_matrix(q, d_code=0x3C00):
+    """Pack an int8 matrix [m][k] as Q8_0 with every scale = d_code."""
+    m, k = q.shape
+    out = bytearray()
+    for r in range(m):
+        for b in range(k // 32):
+            out += bytes([d_code & 0xFF, d_code >> 8]) + q[r, 32 * b:32 * b + 32].astype(np.int8).tobytes()
+    return np.frombuffer(bytes(out), np.uint8)
+
+
+def test_one_hot_permutation_recovers_x():
+    # W[j][c] = [c == perm(j)] with m < k: dst[i][j] must be X[i][perm(j)];
+    # a transposed operand or an off-by-one index fails.
+    m, k, n = 24, 64, 3
+    rng = np.random.default_rng(3)
+    perm = rng.permutation(k)[:m]
+    q = np.zeros((m, k), np.int64)
+    q[np.arange(m), perm] = 1
+    x = rng.uniform(-1, 1, (n, k)).astype(np.float32)
+    dst, am = oracle.matmul("q8_0", _q8_0_matrix(q), x, m, k, n)
+    assert np.array_equal(dst, x[:, perm].astype(np.float64))
+    assert np.array_equal(am, np.abs(x[:, perm]).astype(np.float64))
+
+
+def test_q8_0_unit_scale_equals_integer_matmul():
+    m, k, n = 16, 96, 5
+    rng = np.random.default_rng(11)
+    q = rng.integers(-128, 128, (m, k))
+    x = rng.integers(-8, 9, (n, k)).astype(np.float32)
+    dst, am = oracle.matmul("q8_0", _q8_0_matrix(q), x, m, k, n)
+    want = x.astype(np.int64) @ q.T
+    assert np.array_equal(dst, want.astype(np.float64))
+    assert np.array_equal(am, (np.abs(x.astype(np.int64)) @ np.abs(q).T).astype(np.float64))
+
+
+@pytest.mark.parametrize("fmt,k", [("f32", 32), ("q4_0", 32), ("q8_0", 32), ("q4_k", 256), ("q6_k", 256),
+                                   ("nvfp4", 64)])
+def test_tiny_brute_force_against_library_matmul(fmt, k):
+    import synth
+    m, n = 8, 2
+    w = synth.weights(fmt, m, k, m * oracle.row_bytes(fmt, k))
+    x = synth.activations(n, k)
+    dst, am = oracle.matmul(fmt, w, x, m, k, n)
+    wd = oracle.decode(fmt, w, m, k)
+    want = x.astype(np.float64) @ wd.T
+    assert np.allclose(dst, want, rtol=1e-13, atol=1e-13 * np.abs(want).max())
+    assert np.allclose(am, np.abs(x.astype(np.float64)) @ np.abs(wd).T, rtol=1e-13)
+    ent, ament = oracle.matmul_entries(fmt, w, x, m, k, n, [0, 1, 1], [7, 0, 3])
+    assert np.array_equal(ent, dst[[0, 1, 1], [7, 0, 3]])
+    assert np.array_equal(ament, am[[0, 1, 1], [7, 0, 3]])
+
+
+def test_moe_all_ones_weights_sum_x():
+    # Every scale byte 0x38 (1.0) and every code 2 (1.0): W is all ones, so
+    # y[p][j][r] = scale[p*n_pairs + j] * sum(x[token(j)]).
+    in_f, n_ff, n_used, t = 128, 4, 2, 2
+    n_pairs = t * n_used
+    grp = bytes([0x38] * 4 + [0x22] * 32)
+    mat = np.frombuffer(grp * (n_ff * in_f // 64), np.uint8)
+    mats = [mat] * (2 * n_pairs)
+    scales = np.array([0.5 + 0.01 * p for p in range(2 * n_pairs)], np.float32)
+    x = np.arange(t * in_f, dtype=np.float32).reshape(t, in_f) / 64
+    y, am = oracle.moe_gate_up("nvfp4", mats, scales, x, in_f, n_ff, n_used, t)
+    for p in range(2):
+        for j in range(n_pairs):
+            want = float(scales[p * n_pairs + j]) * float(x[j // n_used].astype(np.float64).sum())
+            assert np.all(y[p, j] == want)
+
+
+def test_moe_matches_per_matrix_products():
+    import synth
+    in_f, n_ff, n_used, t = 128, 16, 3, 1
+    n_pairs = t * n_used
+    mats = [synth.nvfp4_rows(synth.nvfp4_matrix_seed(0, j, p), n_ff, in_f)
+            for p in range(2) for j in range(n_pairs)]
+    scales = np.array([0.5 + 0.01 * p for p in range(2 * n_pairs)], np.float32)
+    x = synth.activations(t, in_f)
+    y, am = oracle.moe_gate_up("nvfp4", mats, scales, x, in_f, n_ff, n_used, t)
+    for p in range(2):
+        for j in range(n_pairs):
+            wd = oracle.decode("nvfp4", mats[p * n_pairs + j], n_ff, in_f)
+            want = float(scales[p * n_pairs + j]) * (wd @ x[0].astype(np.float64))
+            assert np.allclose(y[p, j], want, rtol=1e-13, atol=1e-12)
+    # distinct matrices give distinct outputs (each pair reads its own matrix)
+    assert not np.allclose(y[0, 0], y[0, 1])

@@ -1,0 +1,289 @@
+// decode.cuh -- device decoders of the packed weight formats.
+//
+// Two forms:
+//   decode8<F>   8 consecutive weights of one block -> float32, each equal to
+//                the format's value rounded once to float32 (bit-exact with
+//                the definitions; used by the dequant and GEMV kernels).
+//   decode32_h<F> 32 consecutive weights -> f16 in k order (the A operand of
+//                the tensor-core GEMM).
+//
+// Block layouts (weights per block / bytes per block):
+//   Q4_0 32/18: f16 d, 16 bytes; low nibble of byte j = element j, high
+//               nibble = element j+16; value (q-8)*d.
+//   Q8_0 32/34: f16 d, 32 int8; value q*d.
+//   Q4_K 256/144: f16 d, f16 dmin, 12 bytes of 6-bit scales/mins, 128 bytes of
+//               nibbles; element e: chunk c = e/64, r = e%64, byte 32c + r%32,
+//               low nibble if r < 32; value d*sc*q - dmin*min (ggml k-quant
+//               order).
+//   Q6_K 256/210: 128 B low 4 bits, 64 B high 2 bits, 16 int8 scales, f16 d;
+//               element e: h = e/128, r = e%128, s = r/32, l = r%32, low bits
+//               in byte 64h + l + 32(s&1) (low nibble if s < 2), high bits
+//               (qh[32h+l] >> 2s) & 3, scale 8h + l/16 + 2s; value
+//               d*sc*(q-32).
+//   NVFP4 64/36: 4 E4M3 scale bytes (one per 16), 32 bytes of E2M1 codes,
+//               low nibble of byte j = element 2j; value e2m1*e4m3.
+// (packed sizes: cera 0.4.0 examples/wgpu_gemm_bench.rs, VARIANTS; NVFP4:
+// memra-engine 0.128.0 moe_rows_ceiling_bench.rs, synth_rows.)
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace qmm {
+
+__device__ __forceinline__ uint32_t ldg_u8(const uint8_t *p) { return __ldg(p); }
+__device__ __forceinline__ uint32_t ldg_u16(const uint8_t *p) {
+    return __ldg(reinterpret_cast<const unsigned short *>(p));
+}
+__device__ __forceinline__ uint32_t ldg_u32(const uint8_t *p) {
+    return __ldg(reinterpret_cast<const unsigned int *>(p));
+}
+// 4 bytes from a 2-byte aligned address.
+__device__ __forceinline__ uint32_t ldg_u32_a2(const uint8_t *p) { return ldg_u16(p) | (ldg_u16(p + 2) << 16); }
+
+__device__ __forceinline__ float half_bits_to_f32(uint32_t h) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
+}
+
+// OCP E4M3FN byte -> float (exact; hardware conversion through f16).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
+    __half_raw hr = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(b), __NV_E4M3);
+    return __half2float(__half(hr));
+}
+
+// OCP E2M1 code (4 bits) -> float.  Twice the magnitudes {0,.5,1,1.5,2,3,4,6}
+// are {0,1,2,3,4,6,8,12}, one nibble each of 0xC8643210.
+__device__ __forceinline__ float e2m1_to_f32(uint32_t code) {
+    const float mag = 0.5f * static_cast<float>((0xC8643210u >> (4u * (code & 7u))) & 15u);
+    return (code & 8u) ? -mag : mag;
+}
+
+// Sub-block j (0..7) scale and min of a Q4_K superblock from its 12 scale bytes.
+__device__ __forceinline__ void q4k_sc_min(const uint8_t *sc12, int j, int &sc, int &mn) {
+    if (j < 4) {
+        sc = ldg_u8(sc12 + j) & 63;
+        mn = ldg_u8(sc12 + j + 4) & 63;
+    } else {
+        const uint32_t b = ldg_u8(sc12 + j + 4);
+        sc = static_cast<int>((b & 15u) | ((ldg_u8(sc12 + j - 4) >> 6) << 4));
+        mn = static_cast<int>((b >> 4) | ((ldg_u8(sc12 + j) >> 6) << 4));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// decode8: weights e..e+7 (e % 8 == 0) of the block at `blk`, as float32.
+// `ts` multiplies NVFP4 values after the exact e2m1*e4m3 product.
+// ---------------------------------------------------------------------------
+template <int F> __device__ __forceinline__ void decode8(const uint8_t *blk, int e, float ts, float (&w)[8]);
+
+template <> __device__ __forceinline__ void decode8<QMM_Q4_0>(const uint8_t *blk, int e, float, float (&w)[8]) {
+    const float d = half_bits_to_f32(ldg_u16(blk));
+    const uint8_t *q = blk + 2 + (e & 15);
+    const uint32_t lo = ldg_u32_a2(q), hi = ldg_u32_a2(q + 4);
+    const int sh = (e >= 16) ? 4 : 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        w[j] = static_cast<float>(static_cast<int>((lo >> (8 * j + sh)) & 15u) - 8) * d;
+        w[4 + j] = static_cast<float>(static_cast<int>((hi >> (8 * j + sh)) & 15u) - 8) * d;
+    }
+}
+
+template <> __device__ __forceinline__ void decode8<QMM_Q8_0>(const uint8_t *blk, int e, float, float (&w)[8]) {
+    const float d = half_bits_to_f32(ldg_u16(blk));
+    const uint8_t *q = blk + 2 + e;
+    const uint32_t lo = ldg_u32_a2(q), hi = ldg_u32_a2(q + 4);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        w[j] = static_cast<float>(static_cast<int8_t>((lo >> (8 * j)) & 0xFFu)) * d;
+        w[4 + j] = static_cast<float>(static_cast<int8_t>((hi >> (8 * j)) & 0xFFu)) * d;
+    }
+}
+
+template <> __device__ __forceinline__ void decode8<QMM_Q4_K>(const uint8_t *blk, int e, float, float (&w)[8]) {
+    const uint32_t dd = ldg_u32(blk);
+    const float d = half_bits_to_f32(dd & 0xFFFFu), dmin = half_bits_to_f32(dd >> 16);
+    int sc, mn;
+    q4k_sc_min(blk + 4, e >> 5, sc, mn);
+    const float a = __fmul_rn(d, static_cast<float>(sc));     // exact
+    const float b = __fmul_rn(dmin, static_cast<float>(mn));  // exact
+    const int c = e >> 6, r = e & 63;
+    const uint2 q = __ldg(reinterpret_cast<const uint2 *>(blk + 16 + 32 * c + (r & 31)));
+    const int sh = (r >= 32) ? 4 : 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        w[j] = __fmaf_rn(a, static_cast<float>((q.x >> (8 * j + sh)) & 15u), -b);
+        w[4 + j] = __fmaf_rn(a, static_cast<float>((q.y >> (8 * j + sh)) & 15u), -b);
+    }
+}
+
+template <> __device__ __forceinline__ void decode8<QMM_Q6_K>(const uint8_t *blk, int e, float, float (&w)[8]) {
+    const int h = e >> 7, r = e & 127, s = r >> 5, l = r & 31;
+    const float d = half_bits_to_f32(ldg_u16(blk + 208));
+    const int sc = static_cast<int8_t>(ldg_u8(blk + 192 + 8 * h + (l >> 4) + 2 * s));
+    const float a = __fmul_rn(d, static_cast<float>(sc));  // exact
+    const uint8_t *ql = blk + 64 * h + l + 32 * (s & 1);
+    const uint8_t *qh = blk + 128 + 32 * h + l;
+    const uint32_t ql0 = ldg_u32_a2(ql), ql1 = ldg_u32_a2(ql + 4);
+    const uint32_t qh0 = ldg_u32_a2(qh), qh1 = ldg_u32_a2(qh + 4);
+    const int lsh = (s >= 2) ? 4 : 0, hsh = 2 * s;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int q0 = static_cast<int>(((ql0 >> (8 * j + lsh)) & 15u) | (((qh0 >> (8 * j + hsh)) & 3u) << 4));
+        const int q1 = static_cast<int>(((ql1 >> (8 * j + lsh)) & 15u) | (((qh1 >> (8 * j + hsh)) & 3u) << 4));
+        w[j] = __fmul_rn(a, static_cast<float>(q0 - 32));  // exact
+        w[4 + j] = __fmul_rn(a, static_cast<float>(q1 - 32));
+    }
+}
+
+template <> __device__ __forceinline__ void decode8<QMM_NVFP4>(const uint8_t *blk, int e, float ts, float (&w)[8]) {
+    const float s = e4m3_to_f32(ldg_u8(blk + (e >> 4)));
+    const uint32_t codes = ldg_u32(blk + 4 + (e >> 1));
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float v = __fmul_rn(e2m1_to_f32((codes >> (4 * j)) & 15u), s);  // exact
+        w[j] = __fmul_rn(v, ts);
+    }
+}
+
+// f32 "blocks" are single weights: blk points at weight e of the row... the
+// callers pass the row pointer and the element index instead.
+__device__ __forceinline__ void decode8_f32(const uint8_t *row, int64_t e, int64_t k, float (&w)[8]) {
+    const float *p = reinterpret_cast<const float *>(row) + e;
+    if (e + 8 <= k && (reinterpret_cast<uintptr_t>(p) & 15u) == 0) {
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+        const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+        w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+        w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) w[j] = (e + j < k) ? __ldg(p + j) : 0.0f;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// decode32_h: weights e0..e0+31 of a row (e0 % 32 == 0, one 32-aligned slice
+// inside a block or superblock) as 16 half2 words in k order.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t h2_bits(__half2 v) { return *reinterpret_cast<uint32_t *>(&v); }
+__device__ __forceinline__ __half2 bits_h2(uint32_t v) { return *reinterpret_cast<__half2 *>(&v); }
+
+template <int F> __device__ __forceinline__ void decode32_h(const uint8_t *row, int64_t e0, uint32_t (&o)[16]);
+
+// Q4_0: one whole block.  (1024 + q) is built by OR-ing the nibble into the
+// f16 pattern of 1024.0; subtracting 1032 gives q - 8 exactly; one multiply by
+// d rounds once (round to nearest even).
+template <> __device__ __forceinline__ void decode32_h<QMM_Q4_0>(const uint8_t *row, int64_t e0, uint32_t (&o)[16]) {
+    const uint8_t *blk = row + (e0 >> 5) * 18;
+    const __half2 d2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(ldg_u16(blk))));
+    const __half2 off = __floats2half2_rn(1032.0f, 1032.0f);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const uint32_t v = ldg_u32_a2(blk + 2 + 4 * t);
+        const uint32_t vh = v >> 4;
+        // elements 4t..4t+3 (low nibbles) and 16+4t..16+4t+3 (high nibbles)
+        const uint32_t l01 = (__byte_perm(v, 0, 0x4140) & 0x000F000Fu) | 0x64006400u;
+        const uint32_t l23 = (__byte_perm(v, 0, 0x4342) & 0x000F000Fu) | 0x64006400u;
+        const uint32_t h01 = (__byte_perm(vh, 0, 0x4140) & 0x000F000Fu) | 0x64006400u;
+        const uint32_t h23 = (__byte_perm(vh, 0, 0x4342) & 0x000F000Fu) | 0x64006400u;
+        o[2 * t] = h2_bits(__hmul2(__hsub2(bits_h2(l01), off), d2));
+        o[2 * t + 1] = h2_bits(__hmul2(__hsub2(bits_h2(l23), off), d2));
+        o[8 + 2 * t] = h2_bits(__hmul2(__hsub2(bits_h2(h01), off), d2));
+        o[8 + 2 * t + 1] = h2_bits(__hmul2(__hsub2(bits_h2(h23), off), d2));
+    }
+}
+
+// Q8_0: one whole block.  Flipping the sign bit gives q + 128 as an unsigned
+// byte; placed under the f16 exponent of 1024 it reads 1024 + q + 128, minus
+// 1152 is q exactly; one multiply by d rounds once.
+template <> __device__ __forceinline__ void decode32_h<QMM_Q8_0>(const uint8_t *row, int64_t e0, uint32_t (&o)[16]) {
+    const uint8_t *blk = row + (e0 >> 5) * 34;
+    const __half2 d2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(ldg_u16(blk))));
+    const __half2 off = __floats2half2_rn(1152.0f, 1152.0f);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        const uint32_t v = ldg_u32_a2(blk + 2 + 4 * t) ^ 0x80808080u;
+        const uint32_t p01 = __byte_perm(v, 0x64646464u, 0x4140);
+        const uint32_t p23 = __byte_perm(v, 0x64646464u, 0x4342);
+        o[2 * t] = h2_bits(__hmul2(__hsub2(bits_h2(p01), off), d2));
+        o[2 * t + 1] = h2_bits(__hmul2(__hsub2(bits_h2(p23), off), d2));
+    }
+}
+
+// Q4_K: one 32-weight sub-block, computed in float32 as one fused
+// d*sc*q - dmin*min (both products exact), then rounded to f16.
+template <> __device__ __forceinline__ void decode32_h<QMM_Q4_K>(const uint8_t *row, int64_t e0, uint32_t (&o)[16]) {
+    const uint8_t *blk = row + (e0 >> 8) * 144;
+    const int e = static_cast<int>(e0 & 255);
+    const uint32_t dd = ldg_u32(blk);
+    const float d = half_bits_to_f32(dd & 0xFFFFu), dmin = half_bits_to_f32(dd >> 16);
+    int sc, mn;
+    q4k_sc_min(blk + 4, e >> 5, sc, mn);
+    const float a = __fmul_rn(d, static_cast<float>(sc));
+    const float b = __fmul_rn(dmin, static_cast<float>(mn));
+    const int sh = (e & 32) ? 4 : 0;
+    const uint4 *qp = reinterpret_cast<const uint4 *>(blk + 16 + 32 * (e >> 6));
+    const uint4 q0 = __ldg(qp), q1 = __ldg(qp + 1);
+    const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        const uint32_t v = words[t] >> sh;
+        float f[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) f[j] = __fmaf_rn(a, static_cast<float>((v >> (8 * j)) & 15u), -b);
+        o[2 * t] = h2_bits(__floats2half2_rn(f[0], f[1]));
+        o[2 * t + 1] = h2_bits(__floats2half2_rn(f[2], f[3]));
+    }
+}
+
+// Q6_K: one 32-weight quadrant (h, s); (d*sc)*(q-32) is exact in float32, so
+// the conversion to f16 is the only rounding.
+template <> __device__ __forceinline__ void decode32_h<QMM_Q6_K>(const uint8_t *row, int64_t e0, uint32_t (&o)[16]) {
+    const uint8_t *blk = row + (e0 >> 8) * 210;
+    const int e = static_cast<int>(e0 & 255);
+    const int h = e >> 7, s = (e >> 5) & 3;
+    const float d = half_bits_to_f32(ldg_u16(blk + 208));
+    const uint32_t sc2 = ldg_u16(blk + 192 + 8 * h + 2 * s);
+    const float a0 = __fmul_rn(d, static_cast<float>(static_cast<int8_t>(sc2 & 0xFFu)));
+    const float a1 = __fmul_rn(d, static_cast<float>(static_cast<int8_t>(sc2 >> 8)));
+    const uint8_t *ql = blk + 64 * h + 32 * (s & 1);
+    const uint8_t *qh = blk + 128 + 32 * h;
+    const int lsh = (s >= 2) ? 4 : 0, hsh = 2 * s;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        const uint32_t lo = (ldg_u32_a2(ql + 4 * t) >> lsh) & 0x0F0F0F0Fu;
+        const uint32_t hi = ((ldg_u32_a2(qh + 4 * t) >> hsh) & 0x03030303u) << 4;
+        const uint32_t q = lo | hi;
+        const float a = (t < 4) ? a0 : a1;
+        float f[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) f[j] = __fmul_rn(a, static_cast<float>(static_cast<int>((q >> (8 * j)) & 63u) - 32));
+        o[2 * t] = h2_bits(__floats2half2_rn(f[0], f[1]));
+        o[2 * t + 1] = h2_bits(__floats2half2_rn(f[2], f[3]));
+    }
+}
+
+// NVFP4: half a 64-weight group; e2m1*e4m3 has at most 6 significant bits and
+// lies in [2^-10, 2688], so the f16 product is exact.
+template <> __device__ __forceinline__ void decode32_h<QMM_NVFP4>(const uint8_t *row, int64_t e0, uint32_t (&o)[16]) {
+    const uint8_t *blk = row + (e0 >> 6) * 36;
+    const int half_idx = static_cast<int>((e0 >> 5) & 1);
+    const uint32_t sc2 = ldg_u16(blk + 2 * half_idx);
+    const __half2 s0 = __float2half2_rn(e4m3_to_f32(sc2 & 0xFFu));
+    const __half2 s1 = __float2half2_rn(e4m3_to_f32(sc2 >> 8));
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const uint32_t c = ldg_u32(blk + 4 + 16 * half_idx + 4 * t);
+        const __half2 s = (t < 2) ? s0 : s1;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t byte = (c >> (8 * j)) & 0xFFu;
+            const __half2 v = __floats2half2_rn(e2m1_to_f32(byte & 15u), e2m1_to_f32(byte >> 4));
+            o[4 * t + j] = h2_bits(__hmul2(v, s));
+        }
+    }
+}
+
+}  // namespace qmm

@@ -1,0 +1,77 @@
+// dequant.cu -- standalone packed -> float32 dequant (the dequantize-to-FP32
+// step of the v1 prefill path in aprender-serve 0.70.2 cublas_prefill/mod.rs,
+// module doc).
+//
+// One thread decodes 8 consecutive weights and writes them as two 16-byte
+// stores; the grid strides over the m*k/8 groups.  Bit-exact: every value is
+// the format's value rounded once to float32 (decode.cuh).
+#include "kernels.h"
+#include "decode.cuh"
+
+namespace qmm {
+
+template <int F, typename Idx>
+__global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict__ w, float *__restrict__ out,
+                                                      Idx m, Idx k, Idx rb, float ts) {
+    constexpr int QK = Fmt<F>::QK, BB = Fmt<F>::BB;
+    const Idx gpr = k / 8;  // groups per row
+    const Idx total = m * gpr;
+    for (Idx g = static_cast<Idx>(blockIdx.x) * blockDim.x + threadIdx.x; g < total;
+         g += static_cast<Idx>(gridDim.x) * blockDim.x) {
+        const Idx r = g / gpr;
+        const Idx e0 = (g - r * gpr) * 8;
+        const uint8_t *blk = w + r * rb + (e0 / QK) * BB;
+        float v[8];
+        decode8<F>(blk, static_cast<int>(e0 % QK), ts, v);
+        float4 *o = reinterpret_cast<float4 *>(out + r * k + e0);
+        o[0] = make_float4(v[0], v[1], v[2], v[3]);
+        o[1] = make_float4(v[4], v[5], v[6], v[7]);
+    }
+}
+
+// f32 weights: the decoded value is the weight itself.
+__global__ void __launch_bounds__(256) copy_f32_kernel(const float *__restrict__ w, float *__restrict__ out,
+                                                       int64_t n) {
+    const int64_t n4 = n / 4;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride)
+        reinterpret_cast<float4 *>(out)[i] = __ldg(reinterpret_cast<const float4 *>(w) + i);
+    for (int64_t i = 4 * n4 + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+        out[i] = __ldg(w + i);
+}
+
+template <int F>
+static cudaError_t launch_dequant_t(const void *w, float *out, int64_t m, int64_t k, int64_t rb, float ts,
+                                    int num_sms, cudaStream_t st) {
+    const int64_t total = m * (k / 8);
+    const int64_t want = (total + 255) / 256;
+    const int grid = static_cast<int>(want < 8LL * num_sms ? want : 8LL * num_sms);
+    if (total < (1LL << 31) && m * k < (1LL << 31))
+        dequant_kernel<F, uint32_t><<<grid, 256, 0, st>>>(static_cast<const uint8_t *>(w), out,
+                                                          static_cast<uint32_t>(m), static_cast<uint32_t>(k),
+                                                          static_cast<uint32_t>(rb), ts);
+    else
+        dequant_kernel<F, int64_t><<<grid, 256, 0, st>>>(static_cast<const uint8_t *>(w), out, m, k, rb, ts);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequant(int dtype, const void *w, float *out, int64_t m, int64_t k, int64_t rb, float ts,
+                           int num_sms, cudaStream_t st) {
+    switch (dtype) {
+    case QMM_F32: {
+        const int64_t n = m * k;
+        const int64_t want = (n / 4 + 255) / 256 + 1;
+        const int grid = static_cast<int>(want < 8LL * num_sms ? want : 8LL * num_sms);
+        copy_f32_kernel<<<grid, 256, 0, st>>>(static_cast<const float *>(w), out, n);
+        return cudaGetLastError();
+    }
+    case QMM_Q4_0: return launch_dequant_t<QMM_Q4_0>(w, out, m, k, rb, ts, num_sms, st);
+    case QMM_Q8_0: return launch_dequant_t<QMM_Q8_0>(w, out, m, k, rb, ts, num_sms, st);
+    case QMM_Q4_K: return launch_dequant_t<QMM_Q4_K>(w, out, m, k, rb, ts, num_sms, st);
+    case QMM_Q6_K: return launch_dequant_t<QMM_Q6_K>(w, out, m, k, rb, ts, num_sms, st);
+    case QMM_NVFP4: return launch_dequant_t<QMM_NVFP4>(w, out, m, k, rb, ts, num_sms, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace qmm

@@ -1,0 +1,40 @@
+// kernels.h -- host-side launchers of the qmm kernels (internal to the library).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/qmm.h"
+
+namespace qmm {
+
+cudaError_t launch_dequant(int dtype, const void *w, float *out, int64_t m, int64_t k, int64_t rb, float ts,
+                           int num_sms, cudaStream_t st);
+
+cudaError_t launch_gemv(int dtype, const void *w, int64_t rb, const float *x, float *dst, int64_t m, int64_t k,
+                        int n, int num_sms, cudaStream_t st);
+
+cudaError_t launch_moe_gemv(int dtype, const void *const *w_ptrs, int64_t rb, const float *scales, const float *x,
+                            float *y, int64_t in_f, int64_t n_ff, int n_used, int n_pairs, uint32_t *status,
+                            cudaStream_t st);
+
+// Tensor-core GEMM for n > QMM_GEMV_MAX_N.  x16 is the f16 workspace (packed
+// formats only).  status: the handle's device status word.
+struct GemmArgs {
+    int dtype;
+    const void *w;
+    int64_t rb;
+    const float *x;
+    float *dst;
+    int64_t m, k, n;
+    void *x16;
+    uint32_t *status;
+    uint64_t wait_limit_ns;
+    int debug_skip_first_b_load;  // test hook: leave one stage unloaded so a wait runs out
+};
+cudaError_t launch_gemm_tc(const GemmArgs &a, int num_sms, cudaStream_t st);
+cudaError_t gemm_tc_init();
+
+}  // namespace qmm

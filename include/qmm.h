@@ -1,0 +1,192 @@
+/*
+ * qmm.h -- C ABI of the GB300 (sm_103a) quantized-weight projection matmul.
+ *
+ * The operation is the projection matmul of an LLM layer,
+ *
+ *     dst[n][m] = sum_k W[m][k] * X[n][k],
+ *
+ * the matmul that cera 0.4.0 examples/wgpu_gemm_bench.rs benchmarks (doc
+ * comment of struct Shape: src0 is [m][k], src1 is [n][k], dst is [n][m]),
+ * where W is kept in a packed block-quantized format and decoded inside the
+ * kernels.
+ *
+ * Layouts (all row-major, all dense, no padding between rows):
+ *   W    [m][k] packed: each row is k/QK consecutive blocks of BB bytes
+ *        (qmm_row_bytes), rows back to back.  f32 weights are plain floats.
+ *   X    [n][k] float32, row stride k.
+ *   dst  [n][m] float32, row stride m (m contiguous, as in that page's
+ *        comparison comment on its output stride).
+ *
+ * Block formats (QK weights per block / BB bytes per block), packed sizes as in
+ * the VARIANTS table of the same page and the NVFP4 groups of memra-engine
+ * 0.128.0 src/bin/moe_rows_ceiling_bench.rs, synth_rows:
+ *   QMM_F32    1 / 4     IEEE float32
+ *   QMM_Q4_0   32 / 18   f16 d; 16 bytes, low nibble of byte j = element j,
+ *                        high nibble = element j+16; value (q-8)*d
+ *   QMM_Q8_0   32 / 34   f16 d; 32 int8; value q*d
+ *   QMM_Q4_K  256 / 144  f16 d, f16 dmin, 12 bytes of 6-bit scales/mins for 8
+ *                        sub-blocks of 32, 128 bytes of nibbles;
+ *                        value d*sc*q - dmin*min
+ *   QMM_Q6_K  256 / 210  128 bytes low 4 bits, 64 bytes high 2 bits, 16 int8
+ *                        scales (16 weights each), f16 d; value d*sc*(q-32)
+ *   QMM_NVFP4  64 / 36   4 E4M3 scale bytes (one per 16 weights), 32 bytes of
+ *                        E2M1 codes, low nibble of byte j = element 2j;
+ *                        value e2m1*e4m3
+ * The bit orders inside Q4_K and Q6_K are the ggml k-quant orders.
+ *
+ * Conventions shared by every call:
+ *   - All data pointers are DEVICE pointers owned by the caller; the library
+ *     never frees, keeps or reallocates them.  The handle owns only a 4-byte
+ *     device status word allocated by qmm_create.
+ *   - Pointers must be 16-byte aligned (any cudaMalloc / torch allocation is).
+ *     Packed weight buffers must stay readable up to the next 16-byte boundary
+ *     after their last byte (true of every cudaMalloc allocation).
+ *   - Calls are asynchronous on the caller's stream (a cudaStream_t passed as
+ *     void*, NULL = the legacy default stream).  The return value reports the
+ *     host-side checks and the launch; errors found on the device (a bounded
+ *     wait that expired) are latched in the handle and returned by
+ *     qmm_sync_status.
+ *   - No call allocates device memory after qmm_create, so every call can be
+ *     issued while a stream is being captured into a CUDA graph.
+ *   - Outputs are fully overwritten and are a deterministic function of the
+ *     inputs (no atomics in the arithmetic): two identical calls give
+ *     bit-identical results.
+ *   - Output buffers must not overlap any input buffer.
+ *   - There is no CPU fallback: without an sm_103 device every compute call
+ *     returns an error.
+ */
+#ifndef QMM_H
+#define QMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct qmm_ctx *qmm_handle;
+
+typedef enum {
+    QMM_F32 = 0,
+    QMM_Q4_0 = 1,
+    QMM_Q8_0 = 2,
+    QMM_Q4_K = 3,
+    QMM_Q6_K = 4,
+    QMM_NVFP4 = 5
+} qmm_dtype;
+
+/* Status codes. */
+enum {
+    QMM_OK = 0,
+    QMM_ERR_INVALID_ARG = 1, /* null pointer or handle, unknown dtype       */
+    QMM_ERR_UNSUPPORTED = 2, /* dtype not supported by this call            */
+    QMM_ERR_SHAPE = 3,       /* size out of range or k not a whole block    */
+    QMM_ERR_ALIGN = 4,       /* pointer not 16-byte aligned                 */
+    QMM_ERR_ARCH = 5,        /* device is not sm_103 (GB300)                */
+    QMM_ERR_CUDA = 6,        /* a CUDA runtime call failed                  */
+    QMM_ERR_TIMEOUT = 7,     /* a device-side bounded wait expired          */
+    QMM_ERR_WORKSPACE = 8,   /* workspace missing or too small              */
+    QMM_ERR_OVERLAP = 9      /* an output overlaps an input                 */
+};
+
+/* Largest n that qmm_gemv accepts; qmm_gemm sends n <= this to the same
+ * kernel (the small-batch regime, cf. the GEMM-vs-GEMV threshold of
+ * aprender-serve 0.70.2 cublas_prefill/mod.rs, cublas_gemm_threshold). */
+#define QMM_GEMV_MAX_N 8
+
+/* Create a handle on CUDA device `device`.  Checks that the device is sm_103,
+ * allocates the 4-byte device status word.  *out is set on success only.
+ * Errors: QMM_ERR_INVALID_ARG (out == NULL), QMM_ERR_ARCH, QMM_ERR_CUDA. */
+int qmm_create(int device, qmm_handle *out);
+
+/* Free the handle and its status word.  Waits for nothing: the caller must
+ * not destroy a handle with calls still running.  NULL is accepted. */
+int qmm_destroy(qmm_handle h);
+
+/* Static description of a status code; never NULL. */
+const char *qmm_strerror(int status);
+
+/* QK (weights per block) and BB (bytes per block) of a dtype; 0 if unknown. */
+int64_t qmm_block_weights(qmm_dtype t);
+int64_t qmm_block_bytes(qmm_dtype t);
+
+/* Bytes of one packed row of k weights, k/QK*BB; 0 if k is not a positive
+ * whole number of blocks or t is unknown.  Host-only, needs no device. */
+int64_t qmm_row_bytes(qmm_dtype t, int64_t k);
+
+/* Device workspace, in bytes, that qmm_gemm needs for this problem (0 when it
+ * needs none: n <= QMM_GEMV_MAX_N, or f32 weights).  For the packed formats
+ * at n > QMM_GEMV_MAX_N it holds the f16 copy of X that the tensor-core
+ * kernel reads: n*k*2 bytes rounded up to 256.  Host-only. */
+size_t qmm_gemm_workspace_bytes(qmm_dtype t, int64_t m, int64_t k, int64_t n);
+
+/* dst[n][m] = sum_k W[m][k] * X[n][k]  (cera wgpu_gemm_bench.rs, struct
+ * Shape; the prefill GEMM of its 512-token LFM2 shapes).
+ *   n <= QMM_GEMV_MAX_N: the fp32-FMA GEMV kernel (same as qmm_gemv).
+ *   n >  QMM_GEMV_MAX_N: the tensor-core kernel: packed W is decoded to f16 in
+ *     shared memory, X is rounded to f16 (round to nearest even) into the
+ *     workspace, products accumulate in fp32 in tensor memory (tcgen05
+ *     kind::f16).  f32 W uses kind::tf32 on X and W as given.  Decoded weights
+ *     and X must lie within the f16 range on this path.
+ * Accuracy: |dst - exact| <= 2e-3 * sum_k |W*X| + 1e-6 per element on the
+ * tensor-core path, 1e-5 * sum_k |W*X| on the GEMV path.
+ * Sizes: 1 <= m, n <= 2^24; 1 <= k <= 2^20 and k % QK == 0.  workspace must be
+ * a device buffer of at least qmm_gemm_workspace_bytes(...) bytes (may be NULL
+ * when that is 0).  Errors: QMM_ERR_INVALID_ARG, QMM_ERR_SHAPE,
+ * QMM_ERR_ALIGN, QMM_ERR_WORKSPACE, QMM_ERR_OVERLAP, QMM_ERR_CUDA. */
+int qmm_gemm(qmm_handle h, qmm_dtype t, const void *w, const float *x, float *dst, int64_t m,
+             int64_t k, int64_t n, void *workspace, size_t workspace_bytes, void *stream);
+
+/* The small-batch GEMV: the same product for 1 <= n <= QMM_GEMV_MAX_N, read
+ * straight from the packed weights at their packed size, as the batched
+ * GEMV of aprender-serve 0.70.2 cublas_prefill/mod.rs does (doc comment of
+ * cublas_gemm_threshold).  fp32 decode and fp32 FMA; accuracy
+ * |dst - exact| <= 1e-5 * sum_k |W*X|.  All dtypes.  Errors as qmm_gemm, and
+ * QMM_ERR_SHAPE for n outside 1..QMM_GEMV_MAX_N. */
+int qmm_gemv(qmm_handle h, qmm_dtype t, const void *w, const float *x, float *dst, int64_t m,
+             int64_t k, int64_t n, void *stream);
+
+/* MoE gate/up GEMV over routed experts (memra-engine 0.128.0
+ * src/bin/moe_rows_ceiling_bench.rs: the served gate/up kernel, its pointer
+ * table ptrs[plane*n_pairs + j] and its per-matrix scales scl[pr]).
+ * With n_pairs = t_tokens * n_used, for plane p in {0 = gate, 1 = up} and
+ * pair j < n_pairs (token j / n_used):
+ *   y[p][j][r] = scales[p*n_pairs + j] * sum_c W_pj[r][c] * x[j / n_used][c]
+ * for r < n_ff, where W_pj = w_ptrs[p*n_pairs + j] is an [n_ff][in_f] packed
+ * matrix.  w_ptrs is a DEVICE array of at least 2*n_pairs device pointers
+ * (the page's 3*n_pairs table, whose third plane holds down projections, is
+ * accepted as is; entries past 2*n_pairs are not read).  scales is a device
+ * float array of at least 2*n_pairs entries, x is [t_tokens][in_f] float32,
+ * y is [2][n_pairs][n_ff] float32.  The activation stays fp32 (no int8
+ * re-quantization) and no clamp or gating is applied.  Any dtype; every
+ * matrix pointer must be 16-byte aligned.  Accuracy as qmm_gemv, relative to
+ * |scale| * sum_c |W*x|.  Sizes: 1 <= n_used, t_tokens; n_pairs <= 4096;
+ * 1 <= n_ff <= 2^24; in_f % QK == 0.  Errors as qmm_gemv. */
+int qmm_moe_gemv(qmm_handle h, qmm_dtype t, const void *const *w_ptrs, const float *scales,
+                 const float *x, float *y, int64_t in_f, int64_t n_ff, int n_used, int t_tokens,
+                 void *stream);
+
+/* Standalone dequant (aprender-serve cublas_prefill/mod.rs module doc, v1
+ * path, which dequantizes Q4K/Q6K weights into an FP32 scratch buffer):
+ * out[m][k] float32 = the decoded
+ * value of W[m][k], rounded once to float32; for QMM_NVFP4 the decoded value
+ * times tensor_scale, rounded once (pass 1.0f otherwise; it is ignored for the
+ * other dtypes).  Bit-exact with the formats' definitions.  Sizes as qmm_gemm
+ * (m*k <= 2^40).  Errors: QMM_ERR_INVALID_ARG, QMM_ERR_SHAPE, QMM_ERR_ALIGN,
+ * QMM_ERR_OVERLAP, QMM_ERR_CUDA. */
+int qmm_dequant(qmm_handle h, qmm_dtype t, const void *w, float *out, int64_t m, int64_t k,
+                float tensor_scale, void *stream);
+
+/* Synchronize `stream`, then return and clear the device status latched by
+ * earlier calls on this handle: QMM_OK; QMM_ERR_TIMEOUT (a bounded wait ran
+ * out; that call's output is not valid); QMM_ERR_ALIGN (a qmm_moe_gemv table
+ * entry was NULL or not 16-byte aligned; its rows were set to NaN); or
+ * QMM_ERR_CUDA if the synchronization itself failed. */
+int qmm_sync_status(qmm_handle h, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMM_H */

@@ -13,13 +13,13 @@
  * reordering.  Citations name the page and the item on it:
  *
  *   [cera]   cera 0.4.0, examples/wgpu_gemm_bench.rs
- *              - "One benchmarked matmul: dst[n, m] = src0[m, k] * src1[n, k]"
- *                (doc comment of struct Shape)
+ *              - doc comment of struct Shape: the benchmarked product takes
+ *                src0 [m][k] and src1 [n][k] to dst [n][m]
  *              - VARIANTS table: packed sizes 4 B/weight (f32), 18 B/32
  *                (q4_0), 34 B/32 (q8_0), 144 B/256 (q4_k), 210 B/256 (q6_k)
  *              - fill_quant_bytes doc comment: every f16 scale sits at an even
  *                offset with its high byte at an odd offset
- *              - diff comment: dst is stored with y_stride = m
+ *              - comparison comment in main: dst rows have stride m
  *   [memra]  memra-engine 0.128.0, src/bin/moe_rows_ceiling_bench.rs
  *              - synth_rows: NVFP4 row = in_f/64 groups of 36 B, 4 E4M3 scale
  *                bytes then 32 B of E2M1 nibbles
@@ -27,8 +27,9 @@
  *                scl[pr] = 0.5 + 0.01*pr, gate = plane 0, up = plane 1
  *   [hrx]    hrx-rs patch_bench.rs, fn float: the binary16 decode with
  *              subnormals (exponent field 0 -> mantissa * 2^-24)
- *   [aprender] aprender-serve 0.70.2 cublas_prefill/mod.rs, module doc:
- *              "Dequant Q4K/Q6K -> FP32" (the standalone dequant step)
+ *   [aprender] aprender-serve 0.70.2 cublas_prefill/mod.rs, module doc: its
+ *              v1 prefill path dequantizes weights to FP32 first (the
+ *              standalone dequant step)
  *
  * Readings where the pages are silent (the byte orderings inside Q4_K and
  * Q6_K, the NVFP4 nibble order, the MoE output layout) follow the workload
@@ -292,7 +293,7 @@ int oracle_dequant(int fmt, const uint8_t *w, int64_t m, int64_t k, double tenso
 }
 
 /* ---------------------------------------------------------------------- */
-/* The product ([cera] Shape doc: dst[n, m] = src0[m, k] * src1[n, k])     */
+/* The product ([cera] struct Shape doc comment)                            */
 /* ---------------------------------------------------------------------- */
 
 /* dst[i][j] = sum_c W[j][c] * X[i][c] and absmag[i][j] = sum_c |W[j][c]*X[i][c]|

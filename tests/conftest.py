@@ -34,3 +34,17 @@ def read_golden(name):
             else:
                 blocks.append((int(key), float(rest)))
     return blocks
+
+
+@pytest.fixture(scope="session")
+def h():
+    """One qmm handle on cuda:0 for the GPU tests (fails, never skips, without a GPU)."""
+    import torch
+
+    import gemv_dequant_gemm_gb300 as q
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    torch.cuda.init()
+    handle = q.qmm_create(0)
+    yield handle
+    torch.cuda.synchronize()
+    q.qmm_destroy(handle)

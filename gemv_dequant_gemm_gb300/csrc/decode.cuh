@@ -4,8 +4,8 @@
 //   decode8<F>   8 consecutive weights of one block -> float32, each equal to
 //                the format's value rounded once to float32 (bit-exact with
 //                the definitions; used by the dequant and GEMV kernels).
-//   decode32_h<F> 32 consecutive weights -> f16 in k order (the A operand of
-//                the tensor-core GEMM).
+//   decode32_s<F> 32 consecutive weights staged in shared memory -> f16 in
+//                k order (the A operand of the tensor-core GEMM).
 //
 // Block layouts (weights per block / bytes per block):
 //   Q4_0 32/18: f16 d, 16 bytes; low nibble of byte j = element j, high
@@ -164,25 +164,54 @@ __device__ __forceinline__ void decode8_f32(const uint8_t *row, int64_t e, int64
 }
 
 // ---------------------------------------------------------------------------
-// decode32_h: weights e0..e0+31 of a row (e0 % 32 == 0, one 32-aligned slice
-// inside a block or superblock) as 16 half2 words in k order.
+// decode32_s: weights e0..e0+31 (e0 % 32 == 0) of a raw weight segment staged
+// in shared memory, as 16 half2 words in k order (the A operand of the
+// tensor-core GEMM).  `a` is the shared-memory address of the segment's first
+// block (2-byte aligned); e0 counts from that block.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t h2_bits(__half2 v) { return *reinterpret_cast<uint32_t *>(&v); }
 __device__ __forceinline__ __half2 bits_h2(uint32_t v) { return *reinterpret_cast<__half2 *>(&v); }
 
-template <int F> __device__ __forceinline__ void decode32_h(const uint8_t *row, int64_t e0, uint32_t (&o)[16]);
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint4 lds_v4(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+// N little-endian words starting at any 2-byte aligned shared address:
+// aligned loads, then a funnel shift by the byte offset.
+template <int N> __device__ __forceinline__ void lds_words(uint32_t a, uint32_t (&out)[N]) {
+    const uint32_t base = a & ~3u, sh = (a & 3u) * 8u;
+    uint32_t w[N + 1];
+#pragma unroll
+    for (int i = 0; i <= N; ++i) w[i] = lds_u32(base + 4u * i);
+#pragma unroll
+    for (int i = 0; i < N; ++i) out[i] = __funnelshift_r(w[i], w[i + 1], sh);
+}
+
+template <int F> __device__ __forceinline__ void decode32_s(uint32_t a, int e0, uint32_t (&o)[16]);
 
 // Q4_0: one whole block.  (1024 + q) is built by OR-ing the nibble into the
 // f16 pattern of 1024.0; subtracting 1032 gives q - 8 exactly; one multiply by
 // d rounds once (round to nearest even).
-template <> __device__ __forceinline__ void decode32_h<QMM_Q4_0>(const uint8_t *row, int64_t e0, uint32_t (&o)[16]) {
-    const uint8_t *blk = row + (e0 >> 5) * 18;
-    const __half2 d2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(ldg_u16(blk))));
+template <> __device__ __forceinline__ void decode32_s<QMM_Q4_0>(uint32_t a, int e0, uint32_t (&o)[16]) {
+    const uint32_t blk = a + 18u * static_cast<uint32_t>(e0 >> 5);
+    const __half2 d2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(lds_u16(blk))));
     const __half2 off = __floats2half2_rn(1032.0f, 1032.0f);
+    uint32_t q[4];
+    lds_words<4>(blk + 2, q);
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-        const uint32_t v = ldg_u32_a2(blk + 2 + 4 * t);
-        const uint32_t vh = v >> 4;
+        const uint32_t v = q[t], vh = v >> 4;
         // elements 4t..4t+3 (low nibbles) and 16+4t..16+4t+3 (high nibbles)
         const uint32_t l01 = (__byte_perm(v, 0, 0x4140) & 0x000F000Fu) | 0x64006400u;
         const uint32_t l23 = (__byte_perm(v, 0, 0x4342) & 0x000F000Fu) | 0x64006400u;
@@ -198,90 +227,102 @@ template <> __device__ __forceinline__ void decode32_h<QMM_Q4_0>(const uint8_t *
 // Q8_0: one whole block.  Flipping the sign bit gives q + 128 as an unsigned
 // byte; placed under the f16 exponent of 1024 it reads 1024 + q + 128, minus
 // 1152 is q exactly; one multiply by d rounds once.
-template <> __device__ __forceinline__ void decode32_h<QMM_Q8_0>(const uint8_t *row, int64_t e0, uint32_t (&o)[16]) {
-    const uint8_t *blk = row + (e0 >> 5) * 34;
-    const __half2 d2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(ldg_u16(blk))));
+template <> __device__ __forceinline__ void decode32_s<QMM_Q8_0>(uint32_t a, int e0, uint32_t (&o)[16]) {
+    const uint32_t blk = a + 34u * static_cast<uint32_t>(e0 >> 5);
+    const __half2 d2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(lds_u16(blk))));
     const __half2 off = __floats2half2_rn(1152.0f, 1152.0f);
+    uint32_t q[8];
+    lds_words<8>(blk + 2, q);
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
-        const uint32_t v = ldg_u32_a2(blk + 2 + 4 * t) ^ 0x80808080u;
-        const uint32_t p01 = __byte_perm(v, 0x64646464u, 0x4140);
-        const uint32_t p23 = __byte_perm(v, 0x64646464u, 0x4342);
-        o[2 * t] = h2_bits(__hmul2(__hsub2(bits_h2(p01), off), d2));
-        o[2 * t + 1] = h2_bits(__hmul2(__hsub2(bits_h2(p23), off), d2));
+        const uint32_t v = q[t] ^ 0x80808080u;
+        o[2 * t] = h2_bits(__hmul2(__hsub2(bits_h2(__byte_perm(v, 0x64646464u, 0x4140)), off), d2));
+        o[2 * t + 1] = h2_bits(__hmul2(__hsub2(bits_h2(__byte_perm(v, 0x64646464u, 0x4342)), off), d2));
     }
 }
 
-// Q4_K: one 32-weight sub-block, computed in float32 as one fused
-// d*sc*q - dmin*min (both products exact), then rounded to f16.
-template <> __device__ __forceinline__ void decode32_h<QMM_Q4_K>(const uint8_t *row, int64_t e0, uint32_t (&o)[16]) {
-    const uint8_t *blk = row + (e0 >> 8) * 144;
-    const int e = static_cast<int>(e0 & 255);
-    const uint32_t dd = ldg_u32(blk);
-    const float d = half_bits_to_f32(dd & 0xFFFFu), dmin = half_bits_to_f32(dd >> 16);
-    int sc, mn;
-    q4k_sc_min(blk + 4, e >> 5, sc, mn);
-    const float a = __fmul_rn(d, static_cast<float>(sc));
-    const float b = __fmul_rn(dmin, static_cast<float>(mn));
-    const int sh = (e & 32) ? 4 : 0;
-    const uint4 *qp = reinterpret_cast<const uint4 *>(blk + 16 + 32 * (e >> 6));
-    const uint4 q0 = __ldg(qp), q1 = __ldg(qp + 1);
+// Byte i (0..11, warp-uniform) of the Q4_K scale area held in three words.
+__device__ __forceinline__ uint32_t sc12_byte(uint32_t w0, uint32_t w1, uint32_t w2, int i) {
+    const uint32_t w = i < 4 ? w0 : (i < 8 ? w1 : w2);
+    return (w >> (8 * (i & 3))) & 0xFFu;
+}
+
+// Q4_K: one 32-weight sub-block of the superblock at `a` (16-byte aligned),
+// computed in float32 as one fused d*sc*q - dmin*min (both products exact),
+// then rounded to f16.
+template <> __device__ __forceinline__ void decode32_s<QMM_Q4_K>(uint32_t a, int e0, uint32_t (&o)[16]) {
+    const uint4 hd = lds_v4(a);
+    const float d = half_bits_to_f32(hd.x & 0xFFFFu), dmin = half_bits_to_f32(hd.x >> 16);
+    const int j = e0 >> 5;
+    uint32_t sc, mn;
+    if (j < 4) {
+        sc = sc12_byte(hd.y, hd.z, hd.w, j) & 63u;
+        mn = sc12_byte(hd.y, hd.z, hd.w, j + 4) & 63u;
+    } else {
+        const uint32_t b = sc12_byte(hd.y, hd.z, hd.w, j + 4);
+        sc = (b & 15u) | ((sc12_byte(hd.y, hd.z, hd.w, j - 4) >> 6) << 4);
+        mn = (b >> 4) | ((sc12_byte(hd.y, hd.z, hd.w, j) >> 6) << 4);
+    }
+    const float av = __fmul_rn(d, static_cast<float>(sc));
+    const float bv = __fmul_rn(dmin, static_cast<float>(mn));
+    const int sh = (e0 & 32) ? 4 : 0;
+    const uint32_t qa = a + 16u + 32u * static_cast<uint32_t>(e0 >> 6);
+    const uint4 q0 = lds_v4(qa), q1 = lds_v4(qa + 16u);
     const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
         const uint32_t v = words[t] >> sh;
         float f[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) f[j] = __fmaf_rn(a, static_cast<float>((v >> (8 * j)) & 15u), -b);
+        for (int i = 0; i < 4; ++i) f[i] = __fmaf_rn(av, static_cast<float>((v >> (8 * i)) & 15u), -bv);
         o[2 * t] = h2_bits(__floats2half2_rn(f[0], f[1]));
         o[2 * t + 1] = h2_bits(__floats2half2_rn(f[2], f[3]));
     }
 }
 
-// Q6_K: one 32-weight quadrant (h, s); (d*sc)*(q-32) is exact in float32, so
-// the conversion to f16 is the only rounding.
-template <> __device__ __forceinline__ void decode32_h<QMM_Q6_K>(const uint8_t *row, int64_t e0, uint32_t (&o)[16]) {
-    const uint8_t *blk = row + (e0 >> 8) * 210;
-    const int e = static_cast<int>(e0 & 255);
-    const int h = e >> 7, s = (e >> 5) & 3;
-    const float d = half_bits_to_f32(ldg_u16(blk + 208));
-    const uint32_t sc2 = ldg_u16(blk + 192 + 8 * h + 2 * s);
+// Q6_K: one 32-weight quadrant (h, s) of the superblock at `a`;
+// (d*sc)*(q-32) is exact in float32, so the conversion to f16 is the only
+// rounding.
+template <> __device__ __forceinline__ void decode32_s<QMM_Q6_K>(uint32_t a, int e0, uint32_t (&o)[16]) {
+    const int h = e0 >> 7, s = (e0 >> 5) & 3;
+    const float d = half_bits_to_f32(lds_u16(a + 208u));
+    const uint32_t sc2 = lds_u16(a + 192u + 8u * h + 2u * s);
     const float a0 = __fmul_rn(d, static_cast<float>(static_cast<int8_t>(sc2 & 0xFFu)));
     const float a1 = __fmul_rn(d, static_cast<float>(static_cast<int8_t>(sc2 >> 8)));
-    const uint8_t *ql = blk + 64 * h + 32 * (s & 1);
-    const uint8_t *qh = blk + 128 + 32 * h;
+    uint32_t ql[8], qh[8];
+    lds_words<8>(a + 64u * h + 32u * (s & 1), ql);
+    lds_words<8>(a + 128u + 32u * h, qh);
     const int lsh = (s >= 2) ? 4 : 0, hsh = 2 * s;
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
-        const uint32_t lo = (ldg_u32_a2(ql + 4 * t) >> lsh) & 0x0F0F0F0Fu;
-        const uint32_t hi = ((ldg_u32_a2(qh + 4 * t) >> hsh) & 0x03030303u) << 4;
-        const uint32_t q = lo | hi;
-        const float a = (t < 4) ? a0 : a1;
+        const uint32_t q = ((ql[t] >> lsh) & 0x0F0F0F0Fu) | (((qh[t] >> hsh) & 0x03030303u) << 4);
+        const float av = (t < 4) ? a0 : a1;
         float f[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) f[j] = __fmul_rn(a, static_cast<float>(static_cast<int>((q >> (8 * j)) & 63u) - 32));
+        for (int i = 0; i < 4; ++i) f[i] = __fmul_rn(av, static_cast<float>(static_cast<int>((q >> (8 * i)) & 63u) - 32));
         o[2 * t] = h2_bits(__floats2half2_rn(f[0], f[1]));
         o[2 * t + 1] = h2_bits(__floats2half2_rn(f[2], f[3]));
     }
 }
 
-// NVFP4: half a 64-weight group; e2m1*e4m3 has at most 6 significant bits and
-// lies in [2^-10, 2688], so the f16 product is exact.
-template <> __device__ __forceinline__ void decode32_h<QMM_NVFP4>(const uint8_t *row, int64_t e0, uint32_t (&o)[16]) {
-    const uint8_t *blk = row + (e0 >> 6) * 36;
-    const int half_idx = static_cast<int>((e0 >> 5) & 1);
-    const uint32_t sc2 = ldg_u16(blk + 2 * half_idx);
+// NVFP4: half of the 64-weight group at a + 36*(e0/64) (4-byte aligned);
+// e2m1*e4m3 has at most 6 significant bits and lies in [2^-10, 2688], so the
+// f16 product is exact.
+template <> __device__ __forceinline__ void decode32_s<QMM_NVFP4>(uint32_t a, int e0, uint32_t (&o)[16]) {
+    const uint32_t grp = a + 36u * static_cast<uint32_t>(e0 >> 6);
+    const uint32_t hf = static_cast<uint32_t>((e0 >> 5) & 1);
+    const uint32_t sc2 = lds_u16(grp + 2u * hf);
     const __half2 s0 = __float2half2_rn(e4m3_to_f32(sc2 & 0xFFu));
     const __half2 s1 = __float2half2_rn(e4m3_to_f32(sc2 >> 8));
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-        const uint32_t c = ldg_u32(blk + 4 + 16 * half_idx + 4 * t);
-        const __half2 s = (t < 2) ? s0 : s1;
+        const uint32_t c = lds_u32(grp + 4u + 16u * hf + 4u * t);
+        const __half2 sv = (t < 2) ? s0 : s1;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint32_t byte = (c >> (8 * j)) & 0xFFu;
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t byte = (c >> (8 * i)) & 0xFFu;
             const __half2 v = __floats2half2_rn(e2m1_to_f32(byte & 15u), e2m1_to_f32(byte >> 4));
-            o[4 * t + j] = h2_bits(__hmul2(v, s));
+            o[4 * t + i] = h2_bits(__hmul2(v, sv));
         }
     }
 }

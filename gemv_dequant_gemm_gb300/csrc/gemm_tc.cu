@@ -1,31 +1,42 @@
 // gemm_tc.cu -- the prefill GEMM dst[n][m] = sum_k W[m][k] X[n][k] on the
 // 5th-generation tensor cores (tcgen05), for n > QMM_GEMV_MAX_N.
 //
-// The product is the one of cera 0.4.0 examples/wgpu_gemm_bench.rs (struct
-// Shape: dst[n, m] = src0[m, k] * src1[n, k]; its mul_mat_reg_tile kernel
-// decodes src0 blocks into shared memory with per-format loaders).  Here:
+// The product is the one cera 0.4.0 examples/wgpu_gemm_bench.rs benchmarks
+// (struct Shape; its mul_mat_reg_tile kernel decodes src0 blocks into shared
+// memory with per-format loaders).  Here one CTA owns a 128 (m) x BN (n)
+// output tile and a slice of k:
 //
-//   * X (f32) is rounded once to f16 into the caller's workspace by
-//     x_to_f16_kernel (round to nearest even, like the cvt.rn.f16.f32
-//     converter of aprender-serve cublas_prefill/mod.rs, F32_TO_F16_PTX), and
-//     each CTA streams its [BN x 64] f16 tiles with 2-D TMA in the 128-byte
-//     swizzled K-major layout the MMA reads.
-//   * Packed W is never written back to HBM in decoded form: eight decode
-//     warps read each CTA's [BM x 64] weight slice, decode it to f16
-//     (decode32_h) and store it straight into the same swizzled layout.
-//   * One thread issues tcgen05.mma.kind::f16 (M=128, N=256, K=16; four per
-//     64-wide k stage) with fp32 accumulators in tensor memory (256 columns).
-//     f32 weights skip the decode: TMA loads W and X as f32 and the MMA runs
-//     kind::tf32 (K=8, four per 32-wide stage).
-//   * A 4-stage mbarrier ring couples the roles; tcgen05.commit releases a
-//     stage when the MMAs that read it are done.
-//   * The decode warps then read the accumulator out of TMEM (tcgen05.ld,
-//     32 lanes x 32 columns at a time) and store dst[n][m] with m contiguous,
-//     so every store instruction writes 128 contiguous bytes.
+//   warp 0      raw-weight producer: per-row 1-D bulk copies (TMA) of each
+//               row's packed bytes for 256 k at a time into a ring of raw
+//               stages (16-byte aligned supersets of the rows, so any block
+//               size and row stride works);
+//   warp 1      TMEM allocation and the single MMA-issuing thread:
+//               tcgen05.mma.kind::f16, M=128, N=BN, K=16, four per 64-wide k
+//               stage, fp32 accumulators in BN TMEM columns; tcgen05.commit
+//               releases the stages it read;
+//   warp 2      X producer: 2-D TMA of the f16 copy of X ([BN x 64] tiles,
+//               128-byte swizzle) -- X is rounded once to f16 (round to
+//               nearest even) by x_to_f16_kernel, like the cvt.rn.f16.f32
+//               converter of aprender-serve cublas_prefill/mod.rs;
+//   warps 3-10  decode: each thread turns 32 weights of one row (raw stage in
+//               shared memory) into f16 and stores them in the swizzled
+//               K-major layout the MMA reads -- no decoded weight copy ever
+//               reaches HBM; then the same warps run the epilogue.
 //
-// Every wait is bounded by a wall-clock limit; a wait that runs out latches a
-// status bit, the CTA stops issuing work, waits for its own copies and MMAs
-// in flight, frees its tensor memory and returns.
+// f32 weights skip the decode: warp 2 loads W and X tiles as f32 with TMA and
+// the MMA runs kind::tf32 (K=8, four per 32-wide stage).
+//
+// Split-K: when the output has fewer tiles than the GPU has SMs, S CTAs of a
+// thread-block cluster (dims 1 x 1 x S) share one output tile, each taking a
+// contiguous share of the 256-wide k units.  Each writes its fp32 partial
+// tile to its own shared memory; after a cluster barrier CTA z sums column
+// slice z of all S partials through distributed shared memory in the fixed
+// order 0..S-1 and stores it.  No atomics: the result is deterministic.
+//
+// Every mbarrier wait is bounded by a wall-clock limit; a wait that runs out
+// latches a status bit, the CTA stops issuing work, waits for its own copies
+// and MMAs in flight, frees its tensor memory and returns (after the cluster
+// barriers its peers also pass).
 #include <cudaTypedefs.h>
 #include <string.h>
 
@@ -36,29 +47,54 @@ namespace qmm {
 
 namespace gemm {
 constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int STAGES = 4;
-constexpr int ROWB = 128;                 // bytes of one operand row in one stage
-constexpr int A_STAGE = BM * ROWB;        // 16 KB
-constexpr int B_STAGE = BN * ROWB;        // 32 KB
+constexpr int ROWB = 128;            // bytes of one operand row in one k stage
+constexpr int A_STAGE = BM * ROWB;   // 16 KB
+constexpr int RK = 256;              // k per raw-weight stage and per split-K unit
 constexpr int NUM_DECODE_WARPS = 8;
-constexpr int THREADS = 64 + 32 * NUM_DECODE_WARPS;
-constexpr uint32_t TMEM_COLS = 256;
+constexpr int WARP_RAW = 0, WARP_MMA = 1, WARP_X = 2, WARP_DEC0 = 3;
+constexpr int THREADS = 32 * (WARP_DEC0 + NUM_DECODE_WARPS);  // 352
+constexpr int MAX_SPLIT = 8;
+constexpr int SMEM_LIMIT = 232448;   // 227 KB opt-in per CTA
+constexpr int MAXS = 4;              // ring depth bound (barrier arrays)
 
 struct Ctl {
-    uint64_t full_a[STAGES];  // decode warps finished writing the A stage
-    uint64_t full_b[STAGES];  // TMA bytes of the stage landed
-    uint64_t empty[STAGES];   // the MMAs reading the stage completed
-    uint64_t accum;           // every MMA of the tile completed
+    uint64_t b_full[MAXS], b_empty[MAXS];      // X (and f32 W) tiles
+    uint64_t a_full[MAXS], a_empty[MAXS];      // decoded W tiles
+    uint64_t raw_full[MAXS], raw_empty[MAXS];  // raw weight stages
+    uint64_t accum;
     uint32_t tmem_base;
     int abort;
 };
 
-constexpr size_t SMEM_BYTES = 1024 + STAGES * (A_STAGE + B_STAGE) + sizeof(Ctl);
+// Geometry of a (format, BN) instance: ring depths that fit in shared memory.
+template <int F, int BN> struct Plan {
+    static constexpr bool TF32 = (F == QMM_F32);
+    static constexpr int QK = Fmt<F>::QK, BB = Fmt<F>::BB;
+    static constexpr int KPS = TF32 ? 32 : 64;           // k per MMA stage
+    static constexpr int B_STAGE = BN * ROWB;
+    static constexpr int BS = 4;                          // X-tile stages
+    static constexpr int AS = TF32 ? 4 : 2;               // W-tile stages (f32: loaded with X)
+    // raw stage: 256 k of every row; pitch an odd multiple of 16 bytes >= the
+    // row bytes plus the largest misalignment (block rows are 2-byte aligned)
+    static constexpr int RB = TF32 ? 0 : RK / QK * BB;
+    static constexpr int SLACK = (F == QMM_Q4_K) ? 0 : ((F == QMM_NVFP4) ? 12 : 14);
+    static constexpr int P0 = TF32 ? 16 : (RB + SLACK + 15) / 16 * 16;
+    static constexpr int P = ((P0 / 16) % 2 == 1) ? P0 : P0 + 16;
+    static constexpr int RAW_STAGE = TF32 ? 0 : BM * P;
+    static constexpr int FIXED = BS * B_STAGE + AS * A_STAGE;
+    static constexpr int AVAIL = SMEM_LIMIT - 1024 - static_cast<int>(sizeof(Ctl)) - FIXED;
+    static constexpr int RS0 = TF32 ? 0 : AVAIL / (RAW_STAGE > 0 ? RAW_STAGE : 1);
+    static constexpr int RS = RS0 > 4 ? 4 : RS0;
+    static constexpr int RING = FIXED + RS * RAW_STAGE;
+    static constexpr int RED = BM * BN * 4;               // split-K partial tile (aliases the rings)
+    static constexpr int BODY = RING > RED ? RING : RED;
+    static constexpr size_t SMEM = 1024 + BODY + sizeof(Ctl);
+    static_assert(TF32 || RS >= 2, "raw ring needs two stages");
+    static_assert(SMEM <= SMEM_LIMIT, "shared memory plan too large");
+    static constexpr uint32_t IDESC = mma_idesc(TF32 ? 2u : 0u, BM, BN);
+};
 }  // namespace gemm
 
-// The same wait with no early exit on abort: used where the thing waited for
-// is already in flight (a copy or an MMA) and must land before the CTA ends.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity, uint32_t *status, uint64_t limit_ns) {
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 0;; ++it) {
@@ -70,40 +106,92 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity, 
     }
 }
 
-template <int F>
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ int ld_dsmem_u32(uint32_t addr) {
+    int v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+struct GemmParams {
+    const uint8_t *w;
+    int64_t rb;
+    float *dst;
+    int M, N, K;
+    int units;   // 256-wide k units: ceil(K / 256)
+    int splits;  // CTAs per output tile (cluster size along z)
+    uint32_t *status;
+    uint64_t limit_ns;
+    int debug_skip;
+};
+
+template <int F, int BN>
 __global__ void __launch_bounds__(gemm::THREADS, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ CUtensorMap tmap_a,
-                   const uint8_t *__restrict__ w, int64_t rb, float *__restrict__ dst, int M, int N, int K,
-                   uint32_t *status, uint64_t limit_ns, int debug_skip) {
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
+                   const GemmParams p) {
     using namespace gemm;
-    constexpr bool kTF32 = (F == QMM_F32);
-    constexpr int KPS = kTF32 ? 32 : 64;  // k elements per stage (128 bytes per row)
-    constexpr uint32_t IDESC = mma_idesc(kTF32 ? 2u : 0u, BM, BN);
+    using PL = Plan<F, BN>;
+    constexpr bool TF32 = PL::TF32;
+    constexpr int KPS = PL::KPS, BS = PL::BS, AS = PL::AS, RS = PL::RS;
+    constexpr int SPU = RK / KPS;  // MMA stages per 256-wide unit
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *sA = base;
-    uint8_t *sB = base + STAGES * A_STAGE;
-    Ctl *ctl = reinterpret_cast<Ctl *>(sB + STAGES * B_STAGE);
+    uint8_t *sB = base;
+    uint8_t *sA = sB + BS * PL::B_STAGE;
+    uint8_t *sRaw = sA + AS * A_STAGE;
+    float *sRed = reinterpret_cast<float *>(base);  // split-K partial, after the main loop
+    Ctl *ctl = reinterpret_cast<Ctl *>(base + PL::BODY);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
-    const int KT = (K + KPS - 1) / KPS;
+    const int S = p.splits;
+    const int z = (S > 1) ? static_cast<int>(cluster_rank()) : 0;
+    const int u0 = z * p.units / S, u1 = (z + 1) * p.units / S;
+    const int KT = (p.K + KPS - 1) / KPS;
+    const int kt0 = u0 * SPU;
+    const int kt1 = min(u1 * SPU, KT);
+    const int NK = kt1 - kt0;  // MMA stages of this CTA (>= 1)
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&ctl->full_a[s], NUM_DECODE_WARPS);
-            mbar_init(&ctl->full_b[s], 1);
-            mbar_init(&ctl->empty[s], 1);
+        for (int s = 0; s < MAXS; ++s) {
+            mbar_init(&ctl->b_full[s], 1);
+            mbar_init(&ctl->b_empty[s], 1);
+            mbar_init(&ctl->a_full[s], NUM_DECODE_WARPS);
+            mbar_init(&ctl->a_empty[s], 1);
+            mbar_init(&ctl->raw_full[s], 1);
+            mbar_init(&ctl->raw_empty[s], NUM_DECODE_WARPS);
         }
         mbar_init(&ctl->accum, 1);
         ctl->abort = 0;
         fence_barrier_init();
-        prefetch_tensormap(&tmap_b);
-        if (kTF32) prefetch_tensormap(&tmap_a);
+        prefetch_tensormap(&tmap_x);
+        if (TF32) prefetch_tensormap(&tmap_w);
     }
-    if (warp == 1) {
-        tmem_alloc(&ctl->tmem_base, TMEM_COLS);
+    if (warp == WARP_MMA) {
+        tmem_alloc(&ctl->tmem_base, BN);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -112,81 +200,131 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
     const uint32_t tmem = ctl->tmem_base;
     volatile int *abort = &ctl->abort;
 
-    if (warp == 0) {
-        // ---------------- TMA producer ----------------
-        if (lane == 0) {
-            int last_kt[STAGES];
-            for (int s = 0; s < STAGES; ++s) last_kt[s] = -1;
-            for (int kt = 0; kt < KT; ++kt) {
-                const int s = kt % STAGES;
-                const uint32_t ph = (kt / STAGES) & 1;
-                if (!mbar_wait_bounded(&ctl->empty[s], ph ^ 1, abort, status, limit_ns)) break;
-                if (debug_skip && kt == 0) continue;  // test hook: stage 0 never fills
-                if constexpr (kTF32) {
-                    mbar_arrive_expect_tx(&ctl->full_b[s], A_STAGE + B_STAGE);
-                    tma_load_2d(sA + s * A_STAGE, &tmap_a, kt * KPS, m0, &ctl->full_b[s]);
-                    tma_load_2d(sB + s * B_STAGE, &tmap_b, kt * KPS, n0, &ctl->full_b[s]);
-                } else {
-                    mbar_arrive_expect_tx(&ctl->full_b[s], B_STAGE);
-                    tma_load_2d(sB + s * B_STAGE, &tmap_b, kt * KPS, n0, &ctl->full_b[s]);
+    if (warp == WARP_RAW) {
+        // ------------- raw weight producer (all 32 lanes) -------------
+        if constexpr (!TF32) {
+            int last[RS];
+#pragma unroll
+            for (int r = 0; r < RS; ++r) last[r] = -1;
+            for (int i = 0; u0 + i < u1; ++i) {
+                const int u = u0 + i, r = i % RS;
+                const uint32_t ph = (i / RS) & 1;
+                const bool ok = mbar_wait_bounded(&ctl->raw_empty[r], ph ^ 1, abort, p.status, p.limit_ns);
+                if (!__all_sync(0xFFFFFFFFu, ok)) break;
+                const int64_t seg_off = static_cast<int64_t>(u) * PL::RB;
+                const int len = static_cast<int>(min(static_cast<int64_t>(PL::RB), p.rb - seg_off));
+                uint32_t bytes[4];
+                const uint8_t *src[4];
+                uint32_t tot = 0;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int row = lane + 32 * j, gm = m0 + row;
+                    bytes[j] = 0;
+                    src[j] = nullptr;
+                    if (gm < p.M) {
+                        const uint8_t *s0 = p.w + static_cast<int64_t>(gm) * p.rb + seg_off;
+                        const uintptr_t a = reinterpret_cast<uintptr_t>(s0) & ~uintptr_t(15);
+                        const uint32_t mis = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(s0) - a);
+                        src[j] = reinterpret_cast<const uint8_t *>(a);
+                        bytes[j] = (mis + len + 15u) & ~15u;
+                        tot += bytes[j];
+                    }
                 }
-                last_kt[s] = kt;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xFFFFFFFFu, tot, o);
+                if (lane == 0) mbar_arrive_expect_tx(&ctl->raw_full[r], tot);
+                __syncwarp();
+                uint8_t *stage = sRaw + r * PL::RAW_STAGE;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (bytes[j]) bulk_load_1d(stage + (lane + 32 * j) * PL::P, src[j], bytes[j], &ctl->raw_full[r]);
+                last[r] = i;
+            }
+            if (lane == 0 && *abort) {
+                for (int r = 0; r < RS; ++r)
+                    if (last[r] >= 0) mbar_wait_drain(&ctl->raw_full[r], (last[r] / RS) & 1, p.status, p.limit_ns);
+            }
+            __syncwarp();
+        }
+    } else if (warp == WARP_X) {
+        // ------------- X (and f32 W) tile producer -------------
+        if (lane == 0) {
+            griddep_wait();  // the f16 copy of X is written by the kernel before this one
+            int last[BS];
+#pragma unroll
+            for (int s = 0; s < BS; ++s) last[s] = -1;
+            for (int i = 0; i < NK; ++i) {
+                const int kt = kt0 + i, s = i % BS;
+                const uint32_t ph = (i / BS) & 1;
+                if (!mbar_wait_bounded(&ctl->b_empty[s], ph ^ 1, abort, p.status, p.limit_ns)) break;
+                if (p.debug_skip && i == 0) continue;  // test hook: stage 0 never fills
+                if constexpr (TF32) {
+                    mbar_arrive_expect_tx(&ctl->b_full[s], A_STAGE + PL::B_STAGE);
+                    tma_load_2d(sA + s * A_STAGE, &tmap_w, kt * KPS, m0, &ctl->b_full[s]);
+                } else {
+                    mbar_arrive_expect_tx(&ctl->b_full[s], PL::B_STAGE);
+                }
+                tma_load_2d(sB + s * PL::B_STAGE, &tmap_x, kt * KPS, n0, &ctl->b_full[s]);
+                last[s] = i;
             }
             if (*abort) {
-                // let every copy still in flight land before the CTA ends
-                for (int s = 0; s < STAGES; ++s)
-                    if (last_kt[s] >= 0) mbar_wait_drain(&ctl->full_b[s], (last_kt[s] / STAGES) & 1, status, limit_ns);
+                for (int s = 0; s < BS; ++s)
+                    if (last[s] >= 0) mbar_wait_drain(&ctl->b_full[s], (last[s] / BS) & 1, p.status, p.limit_ns);
             }
         }
-    } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
+        __syncwarp();
+    } else if (warp == WARP_MMA) {
+        // ------------- MMA issuer -------------
         if (lane == 0) {
-            for (int kt = 0; kt < KT; ++kt) {
-                const int s = kt % STAGES;
-                const uint32_t ph = (kt / STAGES) & 1;
-                if (!mbar_wait_bounded(&ctl->full_b[s], ph, abort, status, limit_ns)) break;
-                if (!kTF32 && !mbar_wait_bounded(&ctl->full_a[s], ph, abort, status, limit_ns)) break;
+            for (int i = 0; i < NK; ++i) {
+                const int sb = i % BS, sa = i % AS;
+                if (!mbar_wait_bounded(&ctl->b_full[sb], (i / BS) & 1, abort, p.status, p.limit_ns)) break;
+                if (!TF32 && !mbar_wait_bounded(&ctl->a_full[sa], (i / AS) & 1, abort, p.status, p.limit_ns)) break;
                 tc_fence_after();
-                const uint32_t a_addr = smem_u32(sA + s * A_STAGE);
-                const uint32_t b_addr = smem_u32(sB + s * B_STAGE);
+                const uint32_t a_addr = smem_u32(sA + sa * A_STAGE);
+                const uint32_t b_addr = smem_u32(sB + sb * PL::B_STAGE);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint64_t ad = sw128_desc(a_addr + 32 * kk);
                     const uint64_t bd = sw128_desc(b_addr + 32 * kk);
-                    if constexpr (kTF32)
-                        mma_tf32(tmem, ad, bd, IDESC, (kt | kk) != 0);
+                    if constexpr (TF32)
+                        mma_tf32(tmem, ad, bd, PL::IDESC, (i | kk) != 0);
                     else
-                        mma_f16(tmem, ad, bd, IDESC, (kt | kk) != 0);
+                        mma_f16(tmem, ad, bd, PL::IDESC, (i | kk) != 0);
                 }
-                mma_commit(&ctl->empty[s]);
+                mma_commit(&ctl->b_empty[sb]);
+                if (!TF32) mma_commit(&ctl->a_empty[sa]);
             }
-            // arrives once every MMA issued above has completed
-            mma_commit(&ctl->accum);
+            mma_commit(&ctl->accum);  // arrives once every MMA issued above has completed
         }
         __syncwarp();
     } else {
-        // ---------------- decode warps, then epilogue ----------------
-        const int dt = threadIdx.x - 64;
-        if constexpr (!kTF32) {
+        // ------------- decode warps -------------
+        const int dt = threadIdx.x - 32 * WARP_DEC0;
+        if constexpr (!TF32) {
             const int row = dt & (BM - 1);
-            const int half = dt >> 7;  // which 32 of the stage's 64 k
+            const int half = dt >> 7;  // which 32 of a stage's 64 k
             const int gm = m0 + row;
-            const uint8_t *wrow = w + static_cast<int64_t>(gm < M ? gm : 0) * rb;
-            for (int kt = 0; kt < KT; ++kt) {
-                const int s = kt % STAGES;
-                const uint32_t ph = (kt / STAGES) & 1;
-                // every lane waits; the vote keeps the exit warp-uniform
-                const bool ok = mbar_wait_bounded(&ctl->empty[s], ph ^ 1, abort, status, limit_ns);
+            for (int i = 0; i < NK; ++i) {
+                const int kt = kt0 + i, sa = i % AS;
+                const int ui = kt / SPU - u0, r = ui % RS;  // raw stage of this k stage
+                if (kt % SPU == 0) {
+                    const bool ok = mbar_wait_bounded(&ctl->raw_full[r], (ui / RS) & 1, abort, p.status, p.limit_ns);
+                    if (!__all_sync(0xFFFFFFFFu, ok)) break;
+                }
+                const bool ok = mbar_wait_bounded(&ctl->a_empty[sa], ((i / AS) & 1) ^ 1, abort, p.status, p.limit_ns);
                 if (!__all_sync(0xFFFFFFFFu, ok)) break;
-                const int64_t e0 = static_cast<int64_t>(kt) * 64 + half * 32;
+                const int e_in = (kt % SPU) * 64 + half * 32;  // element within the raw stage
                 uint32_t o[16];
-                if (gm < M && e0 < K) {
-                    decode32_h<F>(wrow, e0, o);
+                if (gm < p.M && static_cast<int64_t>(kt) * 64 + half * 32 < p.K) {
+                    const int64_t seg = static_cast<int64_t>(gm) * p.rb + static_cast<int64_t>(kt / SPU) * PL::RB;
+                    const uint32_t mis = static_cast<uint32_t>((reinterpret_cast<uintptr_t>(p.w) + seg) & 15u);
+                    decode32_s<F>(smem_u32(sRaw + r * PL::RAW_STAGE + row * PL::P) + mis, e_in, o);
                 } else {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) o[j] = 0u;
                 }
-                uint8_t *rowp = sA + s * A_STAGE + (row >> 3) * 1024 + (row & 7) * 128;
+                uint8_t *rowp = sA + sa * A_STAGE + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int c = half * 4 + j;
@@ -195,42 +333,102 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&ctl->full_a[s]);
+                if (lane == 0) {
+                    mbar_arrive(&ctl->a_full[sa]);
+                    if (kt % SPU == SPU - 1 || i == NK - 1) mbar_arrive(&ctl->raw_empty[r]);
+                }
             }
         }
-        // epilogue: wait for the accumulator even after an abort (MMAs may be in flight)
-        const bool drained = mbar_wait_drain(&ctl->accum, 0, status, limit_ns);
-        // tcgen05.ld is warp-collective: decide for the whole warp
-        if (__all_sync(0xFFFFFFFFu, drained && !*abort)) {
+    }
+
+    // ---------------- epilogue ----------------
+    const bool is_epi = warp >= WARP_DEC0;
+    bool have = false;
+    if (is_epi) {
+        const bool drained = mbar_wait_drain(&ctl->accum, 0, p.status, p.limit_ns);
+        if (!drained) *abort = 1;
+        have = __all_sync(0xFFFFFFFFu, drained && !*abort);  // tcgen05.ld is warp-collective
+    }
+    const int q = warp & 3;                                           // TMEM lane quarter of this warp
+    const int colbase = (warp >= WARP_DEC0 + 4) ? BN / 2 : 0;
+    const int rloc = 32 * q + lane;                                   // tile row of this thread
+    if (S == 1) {
+        if (is_epi && have) {
             tc_fence_after();
-            const int q = warp & 3;
-            const int colbase = (warp >= 6) ? BN / 2 : 0;
-            const int gm = m0 + 32 * q + lane;
+            const int gm = m0 + rloc;
 #pragma unroll 1
             for (int c = 0; c < BN / 2 / 32; ++c) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + colbase + 32 * c, v);
                 tmem_ld_wait();
                 const int gn0 = n0 + colbase + 32 * c;
-                if (gm < M) {
+                if (gm < p.M) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        if (gn0 + j < N) dst[static_cast<int64_t>(gn0 + j) * M + gm] = __uint_as_float(v[j]);
+                        if (gn0 + j < p.N) p.dst[static_cast<int64_t>(gn0 + j) * p.M + gm] = __uint_as_float(v[j]);
                 }
             }
         }
+    } else {
+        // partial tile -> own shared memory, column-major [BN][BM]
+        if (is_epi && have) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < BN / 2 / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + colbase + 32 * c, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) sRed[(colbase + 32 * c + j) * BM + rloc] = __uint_as_float(v[j]);
+            }
+        }
+        __syncwarp();
+        cluster_sync_all();
+        // a CTA that gave up left no valid partial: then nobody stores
+        int any_abort = 0;
+        for (int pr = 0; pr < S; ++pr) any_abort |= ld_dsmem_u32(mapa_shared(smem_u32(&ctl->abort), pr));
+        // CTA z sums column slice z of the S partials in rank order and stores it
+        const int cols = BN / S;  // S divides BN (S is a power of two <= 8)
+        const int c0 = z * cols;
+        const uint32_t red0 = smem_u32(sRed);
+        const bool vec = (p.M % 4) == 0;
+        for (int it = any_abort ? THREADS * BN : threadIdx.x; it < cols * (BM / 4); it += THREADS) {
+            const int cl = c0 + it / (BM / 4), r4 = (it % (BM / 4)) * 4;
+            const uint32_t off = static_cast<uint32_t>((cl * BM + r4) * 4);
+            float4 acc = ld_dsmem_v4(mapa_shared(red0 + off, 0));
+            for (int pr = 1; pr < S; ++pr) {
+                const float4 v = ld_dsmem_v4(mapa_shared(red0 + off, static_cast<uint32_t>(pr)));
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
+            const int gn = n0 + cl, gm = m0 + r4;
+            if (gn < p.N && gm < p.M) {
+                float *d = p.dst + static_cast<int64_t>(gn) * p.M + gm;
+                if (vec && gm + 4 <= p.M) {
+                    *reinterpret_cast<float4 *>(d) = acc;
+                } else {
+                    const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+                    for (int t = 0; t < 4 && gm + t < p.M; ++t) d[t] = a4[t];
+                }
+            }
+        }
+        __syncwarp();
+        cluster_sync_all();  // peers keep their partials until every slice is read
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == WARP_MMA) {
         tc_fence_after();
-        tmem_dealloc(tmem, TMEM_COLS);
+        tmem_dealloc(tmem, BN);
     }
 }
 
 // X [n][k] f32 -> [n][k] f16, round to nearest even; k % 8 == 0.
 __global__ void __launch_bounds__(256) x_to_f16_kernel(const float *__restrict__ x, __half *__restrict__ x16,
                                                        int64_t total8) {
+    griddep_launch();  // the GEMM may start staging weights while this runs
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total8; i += stride) {
         const float4 a = __ldg(reinterpret_cast<const float4 *>(x) + 2 * i);
@@ -248,19 +446,19 @@ __global__ void __launch_bounds__(256) x_to_f16_kernel(const float *__restrict__
 static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &qr) ==
                 cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
     }
     return fn;
 }
 
 // 2-D tiled map over a row-major [rows][cols] matrix, box [box_rows][box_cols],
 // 128-byte swizzle (box_cols * elem == 128), zero fill outside the matrix.
-static bool make_map(CUtensorMap *map, const void *base, CUtensorMapDataType dt, int elem, int64_t rows, int64_t cols,
+static bool make_map(CUtensorMap *map, const void *ptr, CUtensorMapDataType dt, int elem, int64_t rows, int64_t cols,
                      int box_rows, int box_cols) {
     auto fn = get_encode_fn();
     if (!fn) return false;
@@ -268,62 +466,108 @@ static bool make_map(CUtensorMap *map, const void *base, CUtensorMapDataType dt,
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * elem};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[2] = {1, 1};
-    return fn(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    return fn(map, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int F>
-static cudaError_t launch_gemm_t(const GemmArgs &a, cudaStream_t st) {
-    using namespace gemm;
-    CUtensorMap map_b, map_a;
-    memset(&map_a, 0, sizeof(map_a));
-    if (F == QMM_F32) {
-        if (!make_map(&map_b, a.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.n, a.k, BN, 32)) return cudaErrorInvalidValue;
-        if (!make_map(&map_a, a.w, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.m, a.k, BM, 32)) return cudaErrorInvalidValue;
-    } else {
-        const int64_t total8 = a.n * a.k / 8;
-        const int64_t want = (total8 + 255) / 256;
-        const int grid = static_cast<int>(want < 1184 ? want : 1184);
-        x_to_f16_kernel<<<grid, 256, 0, st>>>(a.x, static_cast<__half *>(a.x16), total8);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        if (!make_map(&map_b, a.x16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.n, a.k, BN, 64)) return cudaErrorInvalidValue;
-        map_a = map_b;  // unused by the packed-format kernels
-    }
-    const dim3 grid(static_cast<unsigned>((a.m + BM - 1) / BM), static_cast<unsigned>((a.n + BN - 1) / BN));
-    gemm_tc_kernel<F><<<grid, THREADS, SMEM_BYTES, st>>>(map_b, map_a, static_cast<const uint8_t *>(a.w), a.rb, a.dst,
-                                                         static_cast<int>(a.m), static_cast<int>(a.n),
-                                                         static_cast<int>(a.k), a.status, a.wait_limit_ns,
-                                                         a.debug_skip_first_b_load);
-    return cudaGetLastError();
+template <int F, int BN> static cudaError_t set_attr() {
+    return cudaFuncSetAttribute(gemm_tc_kernel<F, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(gemm::Plan<F, BN>::SMEM));
 }
 
-// Opt every instance into the large dynamic shared-memory carve-out; called
-// once per device (with that device current) when a handle is created.
+// Opt every instance into its shared-memory carve-out; called once per device
+// (with that device current) when a handle is created.
 cudaError_t gemm_tc_init() {
-    const int bytes = static_cast<int>(gemm::SMEM_BYTES);
     cudaError_t e = cudaSuccess;
-    auto set = [&](const void *fn) {
-        if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    auto chk = [&](cudaError_t r) {
+        if (e == cudaSuccess) e = r;
     };
-    set(reinterpret_cast<const void *>(gemm_tc_kernel<QMM_F32>));
-    set(reinterpret_cast<const void *>(gemm_tc_kernel<QMM_Q4_0>));
-    set(reinterpret_cast<const void *>(gemm_tc_kernel<QMM_Q8_0>));
-    set(reinterpret_cast<const void *>(gemm_tc_kernel<QMM_Q4_K>));
-    set(reinterpret_cast<const void *>(gemm_tc_kernel<QMM_Q6_K>));
-    set(reinterpret_cast<const void *>(gemm_tc_kernel<QMM_NVFP4>));
+    chk(set_attr<QMM_F32, 128>());
+    chk(set_attr<QMM_Q4_0, 128>());
+    chk(set_attr<QMM_Q8_0, 128>());
+    chk(set_attr<QMM_Q4_K, 128>());
+    chk(set_attr<QMM_Q6_K, 128>());
+    chk(set_attr<QMM_NVFP4, 128>());
     return e;
 }
 
-cudaError_t launch_gemm_tc(const GemmArgs &a, int /*num_sms*/, cudaStream_t st) {
+// Split count: enough CTAs per output tile to cover the SMs, at most one per
+// 256-wide k unit, a power of two up to 8 (it must divide the tile width).
+static int choose_splits(int64_t tiles, int units, int num_sms) {
+    int s = 1;
+    while (s < gemm::MAX_SPLIT && tiles * (s * 2) <= num_sms && s * 2 <= units) s *= 2;
+    return s;
+}
+
+template <int F>
+static cudaError_t launch_gemm_t(const GemmArgs &a, int num_sms, cudaStream_t st) {
+    using namespace gemm;
+    constexpr int BN = 128;
+    using PL = Plan<F, BN>;
+    CUtensorMap map_x, map_w;
+    memset(&map_w, 0, sizeof(map_w));
+    bool pdl = false;
+    if (F == QMM_F32) {
+        if (!make_map(&map_x, a.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.n, a.k, BN, 32)) return cudaErrorInvalidValue;
+        if (!make_map(&map_w, a.w, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.m, a.k, BM, 32)) return cudaErrorInvalidValue;
+    } else {
+        const int64_t total8 = a.n * a.k / 8;
+        const int64_t want = (total8 + 255) / 256;
+        const int grid = static_cast<int>(want < 8LL * num_sms ? want : 8LL * num_sms);
+        x_to_f16_kernel<<<grid, 256, 0, st>>>(a.x, static_cast<__half *>(a.x16), total8);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        if (!make_map(&map_x, a.x16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.n, a.k, BN, 64)) return cudaErrorInvalidValue;
+        map_w = map_x;  // unused by the packed-format kernels
+        pdl = true;
+    }
+    GemmParams p;
+    p.w = static_cast<const uint8_t *>(a.w);
+    p.rb = a.rb;
+    p.dst = a.dst;
+    p.M = static_cast<int>(a.m);
+    p.N = static_cast<int>(a.n);
+    p.K = static_cast<int>(a.k);
+    p.units = static_cast<int>((a.k + RK - 1) / RK);
+    const int64_t tiles = ((a.m + BM - 1) / BM) * ((a.n + BN - 1) / BN);
+    p.splits = choose_splits(tiles, p.units, num_sms);
+    p.status = a.status;
+    p.limit_ns = a.wait_limit_ns;
+    p.debug_skip = a.debug_skip_first_b_load;
+
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(static_cast<unsigned>((a.m + BM - 1) / BM), static_cast<unsigned>((a.n + BN - 1) / BN),
+                       static_cast<unsigned>(p.splits));
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = PL::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    attrs[na].id = cudaLaunchAttributeClusterDimension;
+    attrs[na].val.clusterDim.x = 1;
+    attrs[na].val.clusterDim.y = 1;
+    attrs[na].val.clusterDim.z = static_cast<unsigned>(p.splits);
+    ++na;
+    if (pdl) {
+        attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<F, BN>, map_x, map_w, p);
+}
+
+cudaError_t launch_gemm_tc(const GemmArgs &a, int num_sms, cudaStream_t st) {
     switch (a.dtype) {
-    case QMM_F32: return launch_gemm_t<QMM_F32>(a, st);
-    case QMM_Q4_0: return launch_gemm_t<QMM_Q4_0>(a, st);
-    case QMM_Q8_0: return launch_gemm_t<QMM_Q8_0>(a, st);
-    case QMM_Q4_K: return launch_gemm_t<QMM_Q4_K>(a, st);
-    case QMM_Q6_K: return launch_gemm_t<QMM_Q6_K>(a, st);
-    case QMM_NVFP4: return launch_gemm_t<QMM_NVFP4>(a, st);
+    case QMM_F32: return launch_gemm_t<QMM_F32>(a, num_sms, st);
+    case QMM_Q4_0: return launch_gemm_t<QMM_Q4_0>(a, num_sms, st);
+    case QMM_Q8_0: return launch_gemm_t<QMM_Q8_0>(a, num_sms, st);
+    case QMM_Q4_K: return launch_gemm_t<QMM_Q4_K>(a, num_sms, st);
+    case QMM_Q6_K: return launch_gemm_t<QMM_Q6_K>(a, num_sms, st);
+    case QMM_NVFP4: return launch_gemm_t<QMM_NVFP4>(a, num_sms, st);
     default: return cudaErrorInvalidValue;
     }
 }

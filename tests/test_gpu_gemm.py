@@ -59,7 +59,7 @@ def test_correctness_workload_256x256x16(h, fmt):
     assert_close(got, ref, am, TC_REL, TC_ABS, what=fmt)
 
 
-@pytest.mark.parametrize("m,k,n", [(300, 512, 300), (129, 768, 257), (1, 256, 600), (128, 256, 9), (77, 1280, 513)])
+@pytest.mark.parametrize("m,k,n", [(300, 512, 300), (129, 768, 257), (1, 256, 600), (128, 256, 9), (77, 1280, 513), (100, 2048, 100)])
 @pytest.mark.parametrize("fmt", FORMATS)
 def test_ragged_tiles(h, fmt, m, k, n):
     w, x = weights(fmt, m, k), synth.activations(n, k)

@@ -29,7 +29,7 @@ STATUS = {0: "QMM_OK", 1: "QMM_ERR_INVALID_ARG", 2: "QMM_ERR_UNSUPPORTED", 3: "Q
 # Every symbol include/qmm.h and include/qmm_testing.h declare.
 EXPORTS = ("qmm_create", "qmm_destroy", "qmm_strerror", "qmm_block_weights", "qmm_block_bytes",
            "qmm_row_bytes", "qmm_gemm_workspace_bytes", "qmm_gemm", "qmm_gemv", "qmm_moe_gemv",
-           "qmm_dequant", "qmm_sync_status", "qmm_testing_set_wait_limit_ns",
+           "qmm_dequant", "qmm_sync_status", "qmm_gemm_noalloc", "qmm_testing_set_wait_limit_ns",
            "qmm_testing_skip_first_stage_load")
 
 
@@ -67,6 +67,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "qmm_moe_gemv": (I, [P, I, P, P, P, P, I64, I64, I, I, P]),
         "qmm_dequant": (I, [P, I, P, P, I64, I64, ctypes.c_float, P]),
         "qmm_sync_status": (I, [P, P]),
+        "qmm_gemm_noalloc": (I, [I, P, P, P, I64, I64, I64, P]),
         "qmm_testing_set_wait_limit_ns": (I, [P, ctypes.c_uint64]),
         "qmm_testing_skip_first_stage_load": (I, [P, I]),
     }
@@ -168,6 +169,17 @@ def qmm_dequant(h, t, w, out, m, k, tensor_scale=1.0, stream=None) -> None:
 def qmm_sync_status(h, stream=None) -> int:
     """Synchronize and return the latched device status code (0 = ok); never raises."""
     return load().qmm_sync_status(h, _stream(stream))
+
+
+NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def qmm_gemm_noalloc(t, w, x, dst, m, k, n, stream=None) -> None:
+    """qmm_gemm without a handle or workspace, for callers that cannot allocate
+    device memory; its scratch is a static device array of the library (calls
+    share it, so they must not overlap on the GPU)."""
+    _check(load().qmm_gemm_noalloc(_dt(t), _ptr(w), _ptr(x), _ptr(dst), m, k, n, _stream(stream)),
+           "qmm_gemm_noalloc")
 
 
 def qmm_testing_set_wait_limit_ns(h, limit_ns: int) -> None:

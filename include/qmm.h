@@ -185,6 +185,37 @@ int qmm_dequant(qmm_handle h, qmm_dtype t, const void *w, float *out, int64_t m,
  * QMM_ERR_CUDA if the synchronization itself failed. */
 int qmm_sync_status(qmm_handle h, void *stream);
 
+/* Size of the scratch area that qmm_gemm_noalloc uses: 8 MiB. */
+#define QMM_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* qmm_gemm for callers that cannot allocate device memory: code that runs
+ * where cudaMalloc is unavailable or forbidden (inside a custom allocator or
+ * a memory-pool callback, in a process whose device memory is fully handed
+ * out to another framework, or under a policy that bans allocation after
+ * start-up).  It needs neither a handle (qmm_create allocates a status word)
+ * nor a caller workspace: the f16 copy of X that the tensor-core kernel reads
+ * lives in a static device array of QMM_NOALLOC_SCRATCH_BYTES built into the
+ * library, which every GPU that loads the library holds until the process
+ * exits.  The paper pages have no counterpart of this call.
+ *   - Same product, layouts, accuracy and size rules as qmm_gemm, on the
+ *     current device; n <= QMM_GEMV_MAX_N goes to the GEMV kernel as there.
+ *   - n * k * 2 must not exceed QMM_NOALLOC_SCRATCH_BYTES - 256 when
+ *     n > QMM_GEMV_MAX_N and the weights are packed; larger problems return
+ *     QMM_ERR_WORKSPACE.
+ *   - The first call on a device sets that device up (looks up the scratch
+ *     array's device address, checks the architecture, sets kernel
+ *     attributes); make that first call before any stream capture.
+ *   - Every call shares the one scratch array, whose contents persist from
+ *     call to call: calls that overlap on the GPU (on different streams, or
+ *     from different threads) race on it.  Serialize them.
+ *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ *     routine.  Device-side wait timeouts are latched in the scratch area but
+ *     not reported (there is no handle to report them through).
+ * Errors: QMM_ERR_INVALID_ARG, QMM_ERR_SHAPE, QMM_ERR_ALIGN,
+ * QMM_ERR_OVERLAP, QMM_ERR_WORKSPACE, QMM_ERR_ARCH, QMM_ERR_CUDA. */
+int qmm_gemm_noalloc(qmm_dtype t, const void *w, const float *x, float *dst, int64_t m, int64_t k,
+                     int64_t n, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

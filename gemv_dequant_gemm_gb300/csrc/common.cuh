@@ -74,7 +74,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // *abort and returns false.  Never traps.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, volatile int *abort,
                                                   uint32_t *status, uint64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+    // short waits never touch the (slow) global timer
+    for (int spin = 0; spin < 64; ++spin)
+        if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -86,6 +88,14 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
         }
     }
 }
+
+// Programmatic dependent launch: every kernel of the library is launched with
+// the programmatic-serialization attribute, so it may start while the kernel
+// before it in the stream is still running.  griddep_wait() blocks until that
+// kernel has completed and its memory is visible (a no-op when the launch was
+// ordinary); griddep_launch() lets the next kernel start early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (TMA, tcgen05.mma operand reads).
@@ -209,6 +219,33 @@ __host__ __device__ constexpr uint32_t mma_idesc(uint32_t ab_format, uint32_t m,
            | (ab_format << 10)     // B format
            | ((n >> 3) << 17)      // N / 8
            | ((m >> 4) << 24);     // M / 16
+}
+
+// Launch `kernel` on `st` with programmatic dependent launch allowed (and an
+// optional cluster shape).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              unsigned cluster_z, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (cluster_z > 1) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = 1;
+        attrs[na].val.clusterDim.y = 1;
+        attrs[na].val.clusterDim.z = cluster_z;
+        ++na;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
 }  // namespace qmm

@@ -14,6 +14,8 @@ template <int F, typename Idx>
 __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict__ w, float *__restrict__ out,
                                                       Idx m, Idx k, Idx rb, float ts) {
     constexpr int QK = Fmt<F>::QK, BB = Fmt<F>::BB;
+    griddep_wait();
+    griddep_launch();
     const Idx gpr = k / 8;  // groups per row
     const Idx total = m * gpr;
     for (Idx g = static_cast<Idx>(blockIdx.x) * blockDim.x + threadIdx.x; g < total;
@@ -32,6 +34,8 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict_
 // f32 weights: the decoded value is the weight itself.
 __global__ void __launch_bounds__(256) copy_f32_kernel(const float *__restrict__ w, float *__restrict__ out,
                                                        int64_t n) {
+    griddep_wait();
+    griddep_launch();
     const int64_t n4 = n / 4;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride)
@@ -47,12 +51,10 @@ static cudaError_t launch_dequant_t(const void *w, float *out, int64_t m, int64_
     const int64_t want = (total + 255) / 256;
     const int grid = static_cast<int>(want < 8LL * num_sms ? want : 8LL * num_sms);
     if (total < (1LL << 31) && m * k < (1LL << 31))
-        dequant_kernel<F, uint32_t><<<grid, 256, 0, st>>>(static_cast<const uint8_t *>(w), out,
-                                                          static_cast<uint32_t>(m), static_cast<uint32_t>(k),
-                                                          static_cast<uint32_t>(rb), ts);
-    else
-        dequant_kernel<F, int64_t><<<grid, 256, 0, st>>>(static_cast<const uint8_t *>(w), out, m, k, rb, ts);
-    return cudaGetLastError();
+        return launch_pdl(dequant_kernel<F, uint32_t>, dim3(grid), dim3(256), 0, st, 1u, static_cast<const uint8_t *>(w),
+                          out, static_cast<uint32_t>(m), static_cast<uint32_t>(k), static_cast<uint32_t>(rb), ts);
+    return launch_pdl(dequant_kernel<F, int64_t>, dim3(grid), dim3(256), 0, st, 1u, static_cast<const uint8_t *>(w), out,
+                      m, k, rb, ts);
 }
 
 cudaError_t launch_dequant(int dtype, const void *w, float *out, int64_t m, int64_t k, int64_t rb, float ts,
@@ -62,8 +64,7 @@ cudaError_t launch_dequant(int dtype, const void *w, float *out, int64_t m, int6
         const int64_t n = m * k;
         const int64_t want = (n / 4 + 255) / 256 + 1;
         const int grid = static_cast<int>(want < 8LL * num_sms ? want : 8LL * num_sms);
-        copy_f32_kernel<<<grid, 256, 0, st>>>(static_cast<const float *>(w), out, n);
-        return cudaGetLastError();
+        return launch_pdl(copy_f32_kernel, dim3(grid), dim3(256), 0, st, 1u, static_cast<const float *>(w), out, n);
     }
     case QMM_Q4_0: return launch_dequant_t<QMM_Q4_0>(w, out, m, k, rb, ts, num_sms, st);
     case QMM_Q8_0: return launch_dequant_t<QMM_Q8_0>(w, out, m, k, rb, ts, num_sms, st);

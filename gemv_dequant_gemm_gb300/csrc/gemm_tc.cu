@@ -6,10 +6,11 @@
 // memory with per-format loaders).  Here one CTA owns a 128 (m) x BN (n)
 // output tile and a slice of k:
 //
-//   warp 0      raw-weight producer: per-row 1-D bulk copies (TMA) of each
-//               row's packed bytes for 256 k at a time into a ring of raw
-//               stages (16-byte aligned supersets of the rows, so any block
-//               size and row stride works);
+//   warp 0      raw-weight producer: the packed bytes of 256 k of all 128
+//               rows at a time into a ring of raw stages -- one 2-D TMA box
+//               per stage over the rows viewed as 16-byte aligned row groups
+//               (G rows when G*row_bytes is a multiple of 16), else per-row
+//               1-D bulk copies of 16-byte aligned supersets of each row;
 //   warp 1      TMEM allocation and the single MMA-issuing thread:
 //               tcgen05.mma.kind::f16, M=128, N=BN, K=16, four per 64-wide k
 //               stage, fp32 accumulators in BN TMEM columns; tcgen05.commit
@@ -51,11 +52,13 @@ constexpr int ROWB = 128;            // bytes of one operand row in one k stage
 constexpr int A_STAGE = BM * ROWB;   // 16 KB
 constexpr int RK = 256;              // k per raw-weight stage and per split-K unit
 constexpr int NUM_DECODE_WARPS = 8;
+constexpr int DEC_GROUPS = 4;        // decode warp groups; group g decodes every 4th k stage into A slot g
+constexpr int DEC_GROUP_WARPS = NUM_DECODE_WARPS / DEC_GROUPS;
 constexpr int WARP_RAW = 0, WARP_MMA = 1, WARP_X = 2, WARP_DEC0 = 3;
 constexpr int THREADS = 32 * (WARP_DEC0 + NUM_DECODE_WARPS);  // 352
 constexpr int MAX_SPLIT = 8;
 constexpr int SMEM_LIMIT = 232448;   // 227 KB opt-in per CTA
-constexpr int MAXS = 4;              // ring depth bound (barrier arrays)
+constexpr int MAXS = 8;              // ring depth bound (barrier arrays)
 
 struct Ctl {
     uint64_t b_full[MAXS], b_empty[MAXS];      // X (and f32 W) tiles
@@ -72,8 +75,6 @@ template <int F, int BN> struct Plan {
     static constexpr int QK = Fmt<F>::QK, BB = Fmt<F>::BB;
     static constexpr int KPS = TF32 ? 32 : 64;           // k per MMA stage
     static constexpr int B_STAGE = BN * ROWB;
-    static constexpr int BS = 4;                          // X-tile stages
-    static constexpr int AS = TF32 ? 4 : 2;               // W-tile stages (f32: loaded with X)
     // raw stage: 256 k of every row; pitch an odd multiple of 16 bytes >= the
     // row bytes plus the largest misalignment (block rows are 2-byte aligned)
     static constexpr int RB = TF32 ? 0 : RK / QK * BB;
@@ -81,15 +82,22 @@ template <int F, int BN> struct Plan {
     static constexpr int P0 = TF32 ? 16 : (RB + SLACK + 15) / 16 * 16;
     static constexpr int P = ((P0 / 16) % 2 == 1) ? P0 : P0 + 16;
     static constexpr int RAW_STAGE = TF32 ? 0 : BM * P;
+    static constexpr int RS = TF32 ? 0 : 2;              // raw stages: 8 k stages of look-ahead
+    static constexpr int AVAIL = SMEM_LIMIT - 1024 - static_cast<int>(sizeof(Ctl)) - RS * RAW_STAGE;
+    // packed W: 4 decoded-W stages, as many X stages as fit (at most 8);
+    // f32 W: W and X tiles travel together, as many stages as fit
+    static constexpr int AS0 = TF32 ? AVAIL / (A_STAGE + B_STAGE) : DEC_GROUPS;
+    static constexpr int AS = AS0 > MAXS ? MAXS : AS0;
+    static constexpr int BS0 = TF32 ? AS : (AVAIL - AS * A_STAGE) / B_STAGE;
+    static constexpr int BS = BS0 > MAXS ? MAXS : BS0;
     static constexpr int FIXED = BS * B_STAGE + AS * A_STAGE;
-    static constexpr int AVAIL = SMEM_LIMIT - 1024 - static_cast<int>(sizeof(Ctl)) - FIXED;
-    static constexpr int RS0 = TF32 ? 0 : AVAIL / (RAW_STAGE > 0 ? RAW_STAGE : 1);
-    static constexpr int RS = RS0 > 4 ? 4 : RS0;
     static constexpr int RING = FIXED + RS * RAW_STAGE;
     static constexpr int RED = BM * BN * 4;               // split-K partial tile (aliases the rings)
     static constexpr int BODY = RING > RED ? RING : RED;
     static constexpr size_t SMEM = 1024 + BODY + sizeof(Ctl);
     static_assert(TF32 || RS >= 2, "raw ring needs two stages");
+    static_assert(BS >= 2 && AS >= 2, "rings need two stages");
+    static_assert(TF32 || AS == DEC_GROUPS, "one decoded-W slot per decode group");
     static_assert(SMEM <= SMEM_LIMIT, "shared memory plan too large");
     static constexpr uint32_t IDESC = mma_idesc(TF32 ? 2u : 0u, BM, BN);
 };
@@ -132,8 +140,6 @@ __device__ __forceinline__ int ld_dsmem_u32(uint32_t addr) {
     asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
     return v;
 }
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 struct GemmParams {
     const uint8_t *w;
@@ -141,6 +147,8 @@ struct GemmParams {
     float *dst;
     int M, N, K;
     int units;   // 256-wide k units: ceil(K / 256)
+    int raw_g;   // rows per 16-byte-aligned row group of the raw-weight tensor map; 0 = per-row bulk copies
+    int w_early; // 1: the kernel before this one only wrote the f16 copy of X, so W may be read before it ends
     int splits;  // CTAs per output tile (cluster size along z)
     uint32_t *status;
     uint64_t limit_ns;
@@ -150,7 +158,7 @@ struct GemmParams {
 template <int F, int BN>
 __global__ void __launch_bounds__(gemm::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
-                   const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmap_raw, const GemmParams p) {
     using namespace gemm;
     using PL = Plan<F, BN>;
     constexpr bool TF32 = PL::TF32;
@@ -179,7 +187,7 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
         for (int s = 0; s < MAXS; ++s) {
             mbar_init(&ctl->b_full[s], 1);
             mbar_init(&ctl->b_empty[s], 1);
-            mbar_init(&ctl->a_full[s], NUM_DECODE_WARPS);
+            mbar_init(&ctl->a_full[s], DEC_GROUP_WARPS);
             mbar_init(&ctl->a_empty[s], 1);
             mbar_init(&ctl->raw_full[s], 1);
             mbar_init(&ctl->raw_empty[s], NUM_DECODE_WARPS);
@@ -189,6 +197,7 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
         fence_barrier_init();
         prefetch_tensormap(&tmap_x);
         if (TF32) prefetch_tensormap(&tmap_w);
+        if (!TF32 && p.raw_g > 0) prefetch_tensormap(&tmap_raw);
     }
     if (warp == WARP_MMA) {
         tmem_alloc(&ctl->tmem_base, BN);
@@ -199,6 +208,10 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
     volatile int *abort = &ctl->abort;
+    // everything below may touch memory the previous kernel in the stream
+    // wrote; only the weight producer may skip ahead (see w_early)
+    if (!(warp == WARP_RAW && p.w_early)) griddep_wait();
+    if (threadIdx.x == 0) griddep_launch();
 
     if (warp == WARP_RAW) {
         // ------------- raw weight producer (all 32 lanes) -------------
@@ -212,6 +225,23 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
                 const bool ok = mbar_wait_bounded(&ctl->raw_empty[r], ph ^ 1, abort, p.status, p.limit_ns);
                 if (!__all_sync(0xFFFFFFFFu, ok)) break;
                 const int64_t seg_off = static_cast<int64_t>(u) * PL::RB;
+                if (p.raw_g > 0) {
+                    // one 2-D TMA box per row residue g: rows m0+g, m0+g+G, ... land
+                    // contiguously at slots g*(BM/G) ... with pitch P
+                    if (lane == 0) {
+                        const int G = p.raw_g;
+                        mbar_arrive_expect_tx(&ctl->raw_full[r], BM * PL::P);
+                        uint8_t *stage = sRaw + r * PL::RAW_STAGE;
+                        for (int g = 0; g < G; ++g) {
+                            const int64_t xb = (static_cast<int64_t>(g) * p.rb + seg_off) & ~int64_t(15);
+                            tma_load_2d(stage + g * (BM / G) * PL::P, &tmap_raw, static_cast<int32_t>(xb / 2), m0 / G,
+                                        &ctl->raw_full[r]);
+                        }
+                    }
+                    __syncwarp();
+                    last[r] = i;
+                    continue;
+                }
                 const int len = static_cast<int>(min(static_cast<int64_t>(PL::RB), p.rb - seg_off));
                 uint32_t bytes[4];
                 const uint8_t *src[4];
@@ -249,7 +279,6 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
     } else if (warp == WARP_X) {
         // ------------- X (and f32 W) tile producer -------------
         if (lane == 0) {
-            griddep_wait();  // the f16 copy of X is written by the kernel before this one
             int last[BS];
 #pragma unroll
             for (int s = 0; s < BS; ++s) last[s] = -1;
@@ -300,42 +329,63 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
         __syncwarp();
     } else {
         // ------------- decode warps -------------
-        const int dt = threadIdx.x - 32 * WARP_DEC0;
+        // Group g (two warps) decodes k stages g, g+4, g+8, ... into A slot g,
+        // so four stages are in flight and their barrier round trips overlap.
+        // Each thread turns 4 items of 32 weights (rows tg and tg+64, both
+        // 32-wide halves of the stage) into f16.
         if constexpr (!TF32) {
-            const int row = dt & (BM - 1);
-            const int half = dt >> 7;  // which 32 of a stage's 64 k
-            const int gm = m0 + row;
-            for (int i = 0; i < NK; ++i) {
-                const int kt = kt0 + i, sa = i % AS;
+            const int dt = threadIdx.x - 32 * WARP_DEC0;
+            const int g = dt / (32 * DEC_GROUP_WARPS);
+            const int tg = dt % (32 * DEC_GROUP_WARPS);
+            uint32_t rowoff[2], misb[2];
+            int gmr[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int row = tg + 64 * h;
+                const int slot = (p.raw_g > 0) ? (row % p.raw_g) * (BM / p.raw_g) + row / p.raw_g : row;
+                rowoff[h] = static_cast<uint32_t>(slot * PL::P);
+                gmr[h] = m0 + row;
+                misb[h] = static_cast<uint32_t>(
+                    (reinterpret_cast<uintptr_t>(p.w) + static_cast<int64_t>(gmr[h] < p.M ? gmr[h] : 0) * p.rb) & 15u);
+            }
+            const uint32_t raw0 = smem_u32(sRaw);
+            for (int i = g; i < NK; i += DEC_GROUPS) {
+                const int kt = kt0 + i, sa = g;
                 const int ui = kt / SPU - u0, r = ui % RS;  // raw stage of this k stage
-                if (kt % SPU == 0) {
+                {
                     const bool ok = mbar_wait_bounded(&ctl->raw_full[r], (ui / RS) & 1, abort, p.status, p.limit_ns);
                     if (!__all_sync(0xFFFFFFFFu, ok)) break;
                 }
                 const bool ok = mbar_wait_bounded(&ctl->a_empty[sa], ((i / AS) & 1) ^ 1, abort, p.status, p.limit_ns);
                 if (!__all_sync(0xFFFFFFFFu, ok)) break;
-                const int e_in = (kt % SPU) * 64 + half * 32;  // element within the raw stage
-                uint32_t o[16];
-                if (gm < p.M && static_cast<int64_t>(kt) * 64 + half * 32 < p.K) {
-                    const int64_t seg = static_cast<int64_t>(gm) * p.rb + static_cast<int64_t>(kt / SPU) * PL::RB;
-                    const uint32_t mis = static_cast<uint32_t>((reinterpret_cast<uintptr_t>(p.w) + seg) & 15u);
-                    decode32_s<F>(smem_u32(sRaw + r * PL::RAW_STAGE + row * PL::P) + mis, e_in, o);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) o[j] = 0u;
-                }
-                uint8_t *rowp = sA + sa * A_STAGE + (row >> 3) * 1024 + (row & 7) * 128;
+                const uint32_t useg = static_cast<uint32_t>((kt / SPU) * PL::RB);
+                const uint32_t rawst = raw0 + static_cast<uint32_t>(r * PL::RAW_STAGE);
+                uint8_t *abase = sA + sa * A_STAGE;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const int c = half * 4 + j;
-                    *reinterpret_cast<uint4 *>(rowp + ((c ^ (row & 7)) << 4)) =
-                        make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+                    const int h = j & 1, half = j >> 1;
+                    const int row = tg + 64 * h;
+                    uint32_t o[16];
+                    if (gmr[h] < p.M && static_cast<int64_t>(kt) * 64 + half * 32 < p.K) {
+                        const uint32_t mis = (misb[h] + useg) & 15u;
+                        decode32_s<F>(rawst + rowoff[h] + mis, (kt % SPU) * 64 + half * 32, o);
+                    } else {
+#pragma unroll
+                        for (int q2 = 0; q2 < 16; ++q2) o[q2] = 0u;
+                    }
+                    uint8_t *rowp = abase + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+                    for (int q2 = 0; q2 < 4; ++q2) {
+                        const int c = half * 4 + q2;
+                        *reinterpret_cast<uint4 *>(rowp + ((c ^ (row & 7)) << 4)) =
+                            make_uint4(o[4 * q2], o[4 * q2 + 1], o[4 * q2 + 2], o[4 * q2 + 3]);
+                    }
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&ctl->a_full[sa]);
-                    if (kt % SPU == SPU - 1 || i == NK - 1) mbar_arrive(&ctl->raw_empty[r]);
+                    mbar_arrive(&ctl->raw_empty[r]);  // every group takes one stage of each raw stage
                 }
             }
         }
@@ -428,6 +478,7 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
 // X [n][k] f32 -> [n][k] f16, round to nearest even; k % 8 == 0.
 __global__ void __launch_bounds__(256) x_to_f16_kernel(const float *__restrict__ x, __half *__restrict__ x16,
                                                        int64_t total8) {
+    griddep_wait();    // X may come from the kernel before this one; X16 may still be read by it
     griddep_launch();  // the GEMM may start staging weights while this runs
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total8; i += stride) {
@@ -471,6 +522,26 @@ static bool make_map(CUtensorMap *map, const void *ptr, CUtensorMapDataType dt, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Raw packed-weight map: the [m][rb] bytes viewed as [m/G][G*rb/2] uint16 with
+// G the smallest row group whose byte stride is a multiple of 16; boxes of
+// [BM/G][P/2] (P bytes per row, no swizzle).  Returns G, or 0 when no such
+// view exists (then the kernel copies row by row).
+static int make_raw_map(CUtensorMap *map, const void *w, int64_t m, int64_t rb, int pitch) {
+    auto fn = get_encode_fn();
+    if (!fn) return 0;
+    int G = 1;
+    while (G <= 8 && (G * rb) % 16 != 0) G *= 2;
+    if (G > 8 || m % G != 0 || pitch % 16 != 0 || pitch / 2 > 256) return 0;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(G * rb / 2), static_cast<cuuint64_t>(m / G)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(G * rb)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(pitch / 2), static_cast<cuuint32_t>(gemm::BM / G)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(w), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? G : 0;
+}
+
 template <int F, int BN> static cudaError_t set_attr() {
     return cudaFuncSetAttribute(gemm_tc_kernel<F, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(gemm::Plan<F, BN>::SMEM));
@@ -505,9 +576,11 @@ static cudaError_t launch_gemm_t(const GemmArgs &a, int num_sms, cudaStream_t st
     using namespace gemm;
     constexpr int BN = 128;
     using PL = Plan<F, BN>;
-    CUtensorMap map_x, map_w;
+    CUtensorMap map_x, map_w, map_raw;
     memset(&map_w, 0, sizeof(map_w));
+    memset(&map_raw, 0, sizeof(map_raw));
     bool pdl = false;
+    int raw_g = 0;
     if (F == QMM_F32) {
         if (!make_map(&map_x, a.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.n, a.k, BN, 32)) return cudaErrorInvalidValue;
         if (!make_map(&map_w, a.w, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.m, a.k, BM, 32)) return cudaErrorInvalidValue;
@@ -515,11 +588,12 @@ static cudaError_t launch_gemm_t(const GemmArgs &a, int num_sms, cudaStream_t st
         const int64_t total8 = a.n * a.k / 8;
         const int64_t want = (total8 + 255) / 256;
         const int grid = static_cast<int>(want < 8LL * num_sms ? want : 8LL * num_sms);
-        x_to_f16_kernel<<<grid, 256, 0, st>>>(a.x, static_cast<__half *>(a.x16), total8);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_pdl(x_to_f16_kernel, dim3(grid), dim3(256), 0, st, 1u, a.x,
+                                   static_cast<__half *>(a.x16), total8);
         if (e != cudaSuccess) return e;
         if (!make_map(&map_x, a.x16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.n, a.k, BN, 64)) return cudaErrorInvalidValue;
         map_w = map_x;  // unused by the packed-format kernels
+        raw_g = make_raw_map(&map_raw, a.w, a.m, a.rb, PL::P);
         pdl = true;
     }
     GemmParams p;
@@ -530,34 +604,18 @@ static cudaError_t launch_gemm_t(const GemmArgs &a, int num_sms, cudaStream_t st
     p.N = static_cast<int>(a.n);
     p.K = static_cast<int>(a.k);
     p.units = static_cast<int>((a.k + RK - 1) / RK);
+    p.raw_g = raw_g;
+    p.w_early = pdl ? 1 : 0;
     const int64_t tiles = ((a.m + BM - 1) / BM) * ((a.n + BN - 1) / BN);
     p.splits = choose_splits(tiles, p.units, num_sms);
     p.status = a.status;
     p.limit_ns = a.wait_limit_ns;
     p.debug_skip = a.debug_skip_first_b_load;
 
-    cudaLaunchConfig_t cfg;
-    memset(&cfg, 0, sizeof(cfg));
-    cfg.gridDim = dim3(static_cast<unsigned>((a.m + BM - 1) / BM), static_cast<unsigned>((a.n + BN - 1) / BN),
-                       static_cast<unsigned>(p.splits));
-    cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = PL::SMEM;
-    cfg.stream = st;
-    cudaLaunchAttribute attrs[2];
-    int na = 0;
-    attrs[na].id = cudaLaunchAttributeClusterDimension;
-    attrs[na].val.clusterDim.x = 1;
-    attrs[na].val.clusterDim.y = 1;
-    attrs[na].val.clusterDim.z = static_cast<unsigned>(p.splits);
-    ++na;
-    if (pdl) {
-        attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attrs[na].val.programmaticStreamSerializationAllowed = 1;
-        ++na;
-    }
-    cfg.attrs = attrs;
-    cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<F, BN>, map_x, map_w, p);
+    const dim3 grid(static_cast<unsigned>((a.m + BM - 1) / BM), static_cast<unsigned>((a.n + BN - 1) / BN),
+                    static_cast<unsigned>(p.splits));
+    return launch_pdl(gemm_tc_kernel<F, BN>, grid, dim3(THREADS), PL::SMEM, st, static_cast<unsigned>(p.splits),
+                      map_x, map_w, map_raw, p);
 }
 
 cudaError_t launch_gemm_tc(const GemmArgs &a, int num_sms, cudaStream_t st) {

@@ -107,6 +107,8 @@ __global__ void __launch_bounds__(T) gemv_kernel(const uint8_t *__restrict__ w, 
                                                  const float *__restrict__ x, float *__restrict__ dst, int64_t m,
                                                  int64_t k) {
     __shared__ float red[(T / 32) * R * NV];
+    griddep_wait();
+    griddep_launch();
     const int64_t r0 = static_cast<int64_t>(blockIdx.x) * R;
     const int rows = static_cast<int>(m - r0 < R ? m - r0 : R);
     gemv_body<F, NV, R, T>(w + r0 * rb, rb, x, k, rows, red);
@@ -123,6 +125,8 @@ __global__ void __launch_bounds__(T) moe_gemv_kernel(const void *const *__restri
                                                      float *__restrict__ y, int64_t in_f, int64_t n_ff, int n_used,
                                                      int n_pairs, uint32_t *status) {
     __shared__ float red[(T / 32) * R];
+    griddep_wait();
+    griddep_launch();
     const int mat = blockIdx.y;
     const int pair = mat % n_pairs;
     const int64_t r0 = static_cast<int64_t>(blockIdx.x) * R;
@@ -146,10 +150,8 @@ static cudaError_t launch_gemv_nv(const void *w, int64_t rb, const float *x, flo
     const auto *wb = static_cast<const uint8_t *>(w);
     const unsigned grid = static_cast<unsigned>((m + R - 1) / R);
     if ((k + 7) / 8 <= 128)
-        gemv_kernel<F, NV, R, 128><<<grid, 128, 0, st>>>(wb, rb, x, dst, m, k);
-    else
-        gemv_kernel<F, NV, R, 256><<<grid, 256, 0, st>>>(wb, rb, x, dst, m, k);
-    return cudaGetLastError();
+        return launch_pdl(gemv_kernel<F, NV, R, 128>, dim3(grid), dim3(128), 0, st, 1u, wb, rb, x, dst, m, k);
+    return launch_pdl(gemv_kernel<F, NV, R, 256>, dim3(grid), dim3(256), 0, st, 1u, wb, rb, x, dst, m, k);
 }
 
 template <int F>
@@ -188,10 +190,10 @@ static cudaError_t launch_moe_f(const void *const *w_ptrs, int64_t rb, const flo
     constexpr int R = 4;
     const dim3 grid(static_cast<unsigned>((n_ff + R - 1) / R), static_cast<unsigned>(2 * n_pairs));
     if ((in_f + 7) / 8 <= 128)
-        moe_gemv_kernel<F, R, 128><<<grid, 128, 0, st>>>(w_ptrs, rb, scales, x, y, in_f, n_ff, n_used, n_pairs, status);
-    else
-        moe_gemv_kernel<F, R, 256><<<grid, 256, 0, st>>>(w_ptrs, rb, scales, x, y, in_f, n_ff, n_used, n_pairs, status);
-    return cudaGetLastError();
+        return launch_pdl(moe_gemv_kernel<F, R, 128>, grid, dim3(128), 0, st, 1u, w_ptrs, rb, scales, x, y, in_f, n_ff,
+                          n_used, n_pairs, status);
+    return launch_pdl(moe_gemv_kernel<F, R, 256>, grid, dim3(256), 0, st, 1u, w_ptrs, rb, scales, x, y, in_f, n_ff,
+                      n_used, n_pairs, status);
 }
 
 cudaError_t launch_moe_gemv(int dtype, const void *const *w_ptrs, int64_t rb, const float *scales, const float *x,

@@ -379,18 +379,23 @@ def run_ours(args):
 
 
 def _time_calls(torch, stream, calls, reps):
-    """Mean device time (ms) of calls[i % len(calls)]() over reps launches."""
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    """Mean device time (ms) per call of calls[i % len(calls)]() over reps
+    back-to-back launches: one event pair around the whole run, so that the
+    launches overlap as they do in a model's stream (programmatic dependent
+    launch) and no per-call event splits them.  A device-side sleep queued
+    first keeps the GPU busy while the host enqueues the run."""
     for i in range(min(reps, 3)):
         calls[i % len(calls)]()
     torch.cuda.synchronize()
-    torch.cuda._sleep(2_000_000)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(max(2_000_000, 20_000 * reps))
+    e0.record(stream)
     for i in range(reps):
-        ev[i][0].record(stream)
         calls[i % len(calls)]()
-        ev[i][1].record(stream)
+    e1.record(stream)
     torch.cuda.synchronize()
-    return float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    return e0.elapsed_time(e1) / reps
 
 
 def run_sub_benches(q, lib, h, torch, synth, stream, hbm_gbs):

@@ -163,8 +163,8 @@ int qmm_gemv(qmm_handle h, qmm_dtype t, const void *w, const float *x, float *ds
     if (n > QMM_GEMV_MAX_N) return QMM_ERR_SHAPE;
     const int64_t rb = qmm_row_bytes(t, k);
     return on_device(h, [&] {
-        return qmm::launch_gemv(t, w, rb, x, dst, m, k, static_cast<int>(n), h->num_sms,
-                                static_cast<cudaStream_t>(stream));
+        return qmm::launch_gemv(t, w, rb, x, dst, m, k, static_cast<int>(n), h->num_sms, h->d_status,
+                                h->wait_limit_ns, static_cast<cudaStream_t>(stream));
     });
 }
 
@@ -215,8 +215,8 @@ int qmm_moe_gemv(qmm_handle h, qmm_dtype t, const void *const *w_ptrs, const flo
         return QMM_ERR_OVERLAP;
     const int64_t rb = qmm_row_bytes(t, in_f);
     return on_device(h, [&] {
-        return qmm::launch_moe_gemv(t, w_ptrs, rb, scales, x, y, in_f, n_ff, n_used, n_pairs, h->d_status,
-                                    static_cast<cudaStream_t>(stream));
+        return qmm::launch_moe_gemv(t, w_ptrs, rb, scales, x, y, in_f, n_ff, n_used, n_pairs, t_tokens, h->num_sms,
+                                    h->d_status, h->wait_limit_ns, static_cast<cudaStream_t>(stream));
     });
 }
 

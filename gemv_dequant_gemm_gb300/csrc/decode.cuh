@@ -1,9 +1,10 @@
 // decode.cuh -- device decoders of the packed weight formats.
 //
 // Two forms:
-//   decode8<F>   8 consecutive weights of one block -> float32, each equal to
+//   Dec8<F, L>   8 consecutive weights of one block -> float32, each equal to
 //                the format's value rounded once to float32 (bit-exact with
-//                the definitions; used by the dequant and GEMV kernels).
+//                the definitions; used by the dequant kernel), read through a
+//                global (LdG) or shared-memory (LdS) loader.
 //   decode32_s<F> 32 consecutive weights staged in shared memory -> f16 in
 //                k order (the A operand of the tensor-core GEMM).
 //
@@ -34,16 +35,6 @@
 
 namespace qmm {
 
-__device__ __forceinline__ uint32_t ldg_u8(const uint8_t *p) { return __ldg(p); }
-__device__ __forceinline__ uint32_t ldg_u16(const uint8_t *p) {
-    return __ldg(reinterpret_cast<const unsigned short *>(p));
-}
-__device__ __forceinline__ uint32_t ldg_u32(const uint8_t *p) {
-    return __ldg(reinterpret_cast<const unsigned int *>(p));
-}
-// 4 bytes from a 2-byte aligned address.
-__device__ __forceinline__ uint32_t ldg_u32_a2(const uint8_t *p) { return ldg_u16(p) | (ldg_u16(p + 2) << 16); }
-
 __device__ __forceinline__ float half_bits_to_f32(uint32_t h) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
 }
@@ -61,105 +52,154 @@ __device__ __forceinline__ float e2m1_to_f32(uint32_t code) {
     return (code & 8u) ? -mag : mag;
 }
 
+// Byte loaders: read-only global loads, or shared-memory loads through a
+// generic pointer into shared memory.  The decoders below are written once
+// against either.
+struct LdG {
+    static __device__ __forceinline__ uint32_t u8(const uint8_t *p) { return __ldg(p); }
+    static __device__ __forceinline__ uint32_t u16(const uint8_t *p) {
+        return __ldg(reinterpret_cast<const unsigned short *>(p));
+    }
+    static __device__ __forceinline__ uint32_t u32(const uint8_t *p) {
+        return __ldg(reinterpret_cast<const unsigned int *>(p));
+    }
+    static __device__ __forceinline__ uint2 u64(const uint8_t *p) { return __ldg(reinterpret_cast<const uint2 *>(p)); }
+};
+struct LdS {
+    static __device__ __forceinline__ uint32_t u8(const uint8_t *p) {
+        unsigned short v;
+        asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(smem_u32(p)));
+        return v;
+    }
+    static __device__ __forceinline__ uint32_t u16(const uint8_t *p) {
+        unsigned short v;
+        asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(smem_u32(p)));
+        return v;
+    }
+    static __device__ __forceinline__ uint32_t u32(const uint8_t *p) {
+        uint32_t v;
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)));
+        return v;
+    }
+    static __device__ __forceinline__ uint2 u64(const uint8_t *p) {
+        uint2 v;
+        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(smem_u32(p)));
+        return v;
+    }
+};
+// 4 bytes from a 2-byte aligned address.
+template <class L> __device__ __forceinline__ uint32_t ld_u32_a2(const uint8_t *p) {
+    return L::u16(p) | (L::u16(p + 2) << 16);
+}
+
 // Sub-block j (0..7) scale and min of a Q4_K superblock from its 12 scale bytes.
-__device__ __forceinline__ void q4k_sc_min(const uint8_t *sc12, int j, int &sc, int &mn) {
+template <class L> __device__ __forceinline__ void q4k_sc_min(const uint8_t *sc12, int j, int &sc, int &mn) {
     if (j < 4) {
-        sc = ldg_u8(sc12 + j) & 63;
-        mn = ldg_u8(sc12 + j + 4) & 63;
+        sc = L::u8(sc12 + j) & 63;
+        mn = L::u8(sc12 + j + 4) & 63;
     } else {
-        const uint32_t b = ldg_u8(sc12 + j + 4);
-        sc = static_cast<int>((b & 15u) | ((ldg_u8(sc12 + j - 4) >> 6) << 4));
-        mn = static_cast<int>((b >> 4) | ((ldg_u8(sc12 + j) >> 6) << 4));
+        const uint32_t b = L::u8(sc12 + j + 4);
+        sc = static_cast<int>((b & 15u) | ((L::u8(sc12 + j - 4) >> 6) << 4));
+        mn = static_cast<int>((b >> 4) | ((L::u8(sc12 + j) >> 6) << 4));
     }
 }
 
 // ---------------------------------------------------------------------------
-// decode8: weights e..e+7 (e % 8 == 0) of the block at `blk`, as float32.
-// `ts` multiplies NVFP4 values after the exact e2m1*e4m3 product.
+// Dec8<F, L>::run: weights e..e+7 (e % 8 == 0) of the block at `blk`, as
+// float32.  `ts` multiplies NVFP4 values after the exact e2m1*e4m3 product.
 // ---------------------------------------------------------------------------
-template <int F> __device__ __forceinline__ void decode8(const uint8_t *blk, int e, float ts, float (&w)[8]);
+template <int F, class L> struct Dec8;
 
-template <> __device__ __forceinline__ void decode8<QMM_Q4_0>(const uint8_t *blk, int e, float, float (&w)[8]) {
-    const float d = half_bits_to_f32(ldg_u16(blk));
-    const uint8_t *q = blk + 2 + (e & 15);
-    const uint32_t lo = ldg_u32_a2(q), hi = ldg_u32_a2(q + 4);
-    const int sh = (e >= 16) ? 4 : 0;
+template <class L> struct Dec8<QMM_Q4_0, L> {
+    static __device__ __forceinline__ void run(const uint8_t *blk, int e, float, float (&w)[8]) {
+        const float d = half_bits_to_f32(L::u16(blk));
+        const uint8_t *q = blk + 2 + (e & 15);
+        const uint32_t lo = ld_u32_a2<L>(q), hi = ld_u32_a2<L>(q + 4);
+        const int sh = (e >= 16) ? 4 : 0;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        w[j] = static_cast<float>(static_cast<int>((lo >> (8 * j + sh)) & 15u) - 8) * d;
-        w[4 + j] = static_cast<float>(static_cast<int>((hi >> (8 * j + sh)) & 15u) - 8) * d;
+        for (int j = 0; j < 4; ++j) {
+            w[j] = static_cast<float>(static_cast<int>((lo >> (8 * j + sh)) & 15u) - 8) * d;
+            w[4 + j] = static_cast<float>(static_cast<int>((hi >> (8 * j + sh)) & 15u) - 8) * d;
+        }
     }
-}
+};
 
-template <> __device__ __forceinline__ void decode8<QMM_Q8_0>(const uint8_t *blk, int e, float, float (&w)[8]) {
-    const float d = half_bits_to_f32(ldg_u16(blk));
-    const uint8_t *q = blk + 2 + e;
-    const uint32_t lo = ldg_u32_a2(q), hi = ldg_u32_a2(q + 4);
+template <class L> struct Dec8<QMM_Q8_0, L> {
+    static __device__ __forceinline__ void run(const uint8_t *blk, int e, float, float (&w)[8]) {
+        const float d = half_bits_to_f32(L::u16(blk));
+        const uint8_t *q = blk + 2 + e;
+        const uint32_t lo = ld_u32_a2<L>(q), hi = ld_u32_a2<L>(q + 4);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        w[j] = static_cast<float>(static_cast<int8_t>((lo >> (8 * j)) & 0xFFu)) * d;
-        w[4 + j] = static_cast<float>(static_cast<int8_t>((hi >> (8 * j)) & 0xFFu)) * d;
+        for (int j = 0; j < 4; ++j) {
+            w[j] = static_cast<float>(static_cast<int8_t>((lo >> (8 * j)) & 0xFFu)) * d;
+            w[4 + j] = static_cast<float>(static_cast<int8_t>((hi >> (8 * j)) & 0xFFu)) * d;
+        }
     }
-}
+};
 
-template <> __device__ __forceinline__ void decode8<QMM_Q4_K>(const uint8_t *blk, int e, float, float (&w)[8]) {
-    const uint32_t dd = ldg_u32(blk);
-    const float d = half_bits_to_f32(dd & 0xFFFFu), dmin = half_bits_to_f32(dd >> 16);
-    int sc, mn;
-    q4k_sc_min(blk + 4, e >> 5, sc, mn);
-    const float a = __fmul_rn(d, static_cast<float>(sc));     // exact
-    const float b = __fmul_rn(dmin, static_cast<float>(mn));  // exact
-    const int c = e >> 6, r = e & 63;
-    const uint2 q = __ldg(reinterpret_cast<const uint2 *>(blk + 16 + 32 * c + (r & 31)));
-    const int sh = (r >= 32) ? 4 : 0;
+template <class L> struct Dec8<QMM_Q4_K, L> {
+    static __device__ __forceinline__ void run(const uint8_t *blk, int e, float, float (&w)[8]) {
+        const uint32_t dd = L::u32(blk);
+        const float d = half_bits_to_f32(dd & 0xFFFFu), dmin = half_bits_to_f32(dd >> 16);
+        int sc, mn;
+        q4k_sc_min<L>(blk + 4, e >> 5, sc, mn);
+        const float a = __fmul_rn(d, static_cast<float>(sc));     // exact
+        const float b = __fmul_rn(dmin, static_cast<float>(mn));  // exact
+        const int c = e >> 6, r = e & 63;
+        const uint2 q = L::u64(blk + 16 + 32 * c + (r & 31));
+        const int sh = (r >= 32) ? 4 : 0;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        w[j] = __fmaf_rn(a, static_cast<float>((q.x >> (8 * j + sh)) & 15u), -b);
-        w[4 + j] = __fmaf_rn(a, static_cast<float>((q.y >> (8 * j + sh)) & 15u), -b);
+        for (int j = 0; j < 4; ++j) {
+            w[j] = __fmaf_rn(a, static_cast<float>((q.x >> (8 * j + sh)) & 15u), -b);
+            w[4 + j] = __fmaf_rn(a, static_cast<float>((q.y >> (8 * j + sh)) & 15u), -b);
+        }
     }
-}
+};
 
-template <> __device__ __forceinline__ void decode8<QMM_Q6_K>(const uint8_t *blk, int e, float, float (&w)[8]) {
-    const int h = e >> 7, r = e & 127, s = r >> 5, l = r & 31;
-    const float d = half_bits_to_f32(ldg_u16(blk + 208));
-    const int sc = static_cast<int8_t>(ldg_u8(blk + 192 + 8 * h + (l >> 4) + 2 * s));
-    const float a = __fmul_rn(d, static_cast<float>(sc));  // exact
-    const uint8_t *ql = blk + 64 * h + l + 32 * (s & 1);
-    const uint8_t *qh = blk + 128 + 32 * h + l;
-    const uint32_t ql0 = ldg_u32_a2(ql), ql1 = ldg_u32_a2(ql + 4);
-    const uint32_t qh0 = ldg_u32_a2(qh), qh1 = ldg_u32_a2(qh + 4);
-    const int lsh = (s >= 2) ? 4 : 0, hsh = 2 * s;
+template <class L> struct Dec8<QMM_Q6_K, L> {
+    static __device__ __forceinline__ void run(const uint8_t *blk, int e, float, float (&w)[8]) {
+        const int h = e >> 7, r = e & 127, s = r >> 5, l = r & 31;
+        const float d = half_bits_to_f32(L::u16(blk + 208));
+        const int sc = static_cast<int8_t>(L::u8(blk + 192 + 8 * h + (l >> 4) + 2 * s));
+        const float a = __fmul_rn(d, static_cast<float>(sc));  // exact
+        const uint8_t *ql = blk + 64 * h + l + 32 * (s & 1);
+        const uint8_t *qh = blk + 128 + 32 * h + l;
+        const uint32_t ql0 = ld_u32_a2<L>(ql), ql1 = ld_u32_a2<L>(ql + 4);
+        const uint32_t qh0 = ld_u32_a2<L>(qh), qh1 = ld_u32_a2<L>(qh + 4);
+        const int lsh = (s >= 2) ? 4 : 0, hsh = 2 * s;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int q0 = static_cast<int>(((ql0 >> (8 * j + lsh)) & 15u) | (((qh0 >> (8 * j + hsh)) & 3u) << 4));
-        const int q1 = static_cast<int>(((ql1 >> (8 * j + lsh)) & 15u) | (((qh1 >> (8 * j + hsh)) & 3u) << 4));
-        w[j] = __fmul_rn(a, static_cast<float>(q0 - 32));  // exact
-        w[4 + j] = __fmul_rn(a, static_cast<float>(q1 - 32));
+        for (int j = 0; j < 4; ++j) {
+            const int q0 = static_cast<int>(((ql0 >> (8 * j + lsh)) & 15u) | (((qh0 >> (8 * j + hsh)) & 3u) << 4));
+            const int q1 = static_cast<int>(((ql1 >> (8 * j + lsh)) & 15u) | (((qh1 >> (8 * j + hsh)) & 3u) << 4));
+            w[j] = __fmul_rn(a, static_cast<float>(q0 - 32));  // exact
+            w[4 + j] = __fmul_rn(a, static_cast<float>(q1 - 32));
+        }
     }
-}
+};
 
-template <> __device__ __forceinline__ void decode8<QMM_NVFP4>(const uint8_t *blk, int e, float ts, float (&w)[8]) {
-    const float s = e4m3_to_f32(ldg_u8(blk + (e >> 4)));
-    const uint32_t codes = ldg_u32(blk + 4 + (e >> 1));
+template <class L> struct Dec8<QMM_NVFP4, L> {
+    static __device__ __forceinline__ void run(const uint8_t *blk, int e, float ts, float (&w)[8]) {
+        const float s = e4m3_to_f32(L::u8(blk + (e >> 4)));
+        const uint32_t codes = L::u32(blk + 4 + (e >> 1));
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const float v = __fmul_rn(e2m1_to_f32((codes >> (4 * j)) & 15u), s);  // exact
-        w[j] = __fmul_rn(v, ts);
+        for (int j = 0; j < 8; ++j) {
+            const float v = __fmul_rn(e2m1_to_f32((codes >> (4 * j)) & 15u), s);  // exact
+            w[j] = __fmul_rn(v, ts);
+        }
     }
-}
+};
 
-// f32 "blocks" are single weights: blk points at weight e of the row... the
-// callers pass the row pointer and the element index instead.
-__device__ __forceinline__ void decode8_f32(const uint8_t *row, int64_t e, int64_t k, float (&w)[8]) {
-    const float *p = reinterpret_cast<const float *>(row) + e;
-    if (e + 8 <= k && (reinterpret_cast<uintptr_t>(p) & 15u) == 0) {
-        const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
-        const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
-        w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
-        w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+// f32 weights: 8 consecutive weights of a row from element e (bounds-checked
+// against k); `row` points at the row's first weight.
+template <class L> __device__ __forceinline__ void decode8_f32(const uint8_t *row, int64_t e, int64_t k, float (&w)[8]) {
+    const uint8_t *p = row + 4 * e;
+    if (e + 8 <= k && (reinterpret_cast<uintptr_t>(p) & 7u) == 0) {
+        const uint2 a = L::u64(p), b = L::u64(p + 8), c = L::u64(p + 16), d = L::u64(p + 24);
+        w[0] = __uint_as_float(a.x); w[1] = __uint_as_float(a.y); w[2] = __uint_as_float(b.x); w[3] = __uint_as_float(b.y);
+        w[4] = __uint_as_float(c.x); w[5] = __uint_as_float(c.y); w[6] = __uint_as_float(d.x); w[7] = __uint_as_float(d.y);
     } else {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) w[j] = (e + j < k) ? __ldg(p + j) : 0.0f;
+        for (int j = 0; j < 8; ++j) w[j] = (e + j < k) ? __uint_as_float(L::u32(p + 4 * j)) : 0.0f;
     }
 }
 

@@ -24,7 +24,7 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict_
         const Idx e0 = (g - r * gpr) * 8;
         const uint8_t *blk = w + r * rb + (e0 / QK) * BB;
         float v[8];
-        decode8<F>(blk, static_cast<int>(e0 % QK), ts, v);
+        Dec8<F, LdG>::run(blk, static_cast<int>(e0 % QK), ts, v);
         float4 *o = reinterpret_cast<float4 *>(out + r * k + e0);
         o[0] = make_float4(v[0], v[1], v[2], v[3]);
         o[1] = make_float4(v[4], v[5], v[6], v[7]);

@@ -13,12 +13,15 @@ namespace qmm {
 cudaError_t launch_dequant(int dtype, const void *w, float *out, int64_t m, int64_t k, int64_t rb, float ts,
                            int num_sms, cudaStream_t st);
 
+// Small-batch GEMV (1 <= n <= 8).  status: device status word; limit_ns:
+// the bound on every wait inside the kernel.
 cudaError_t launch_gemv(int dtype, const void *w, int64_t rb, const float *x, float *dst, int64_t m, int64_t k,
-                        int n, int num_sms, cudaStream_t st);
+                        int n, int num_sms, uint32_t *status, uint64_t limit_ns, cudaStream_t st);
 
+// MoE gate/up GEMV over 2 * n_pairs matrices; tokens = rows of x.
 cudaError_t launch_moe_gemv(int dtype, const void *const *w_ptrs, int64_t rb, const float *scales, const float *x,
-                            float *y, int64_t in_f, int64_t n_ff, int n_used, int n_pairs, uint32_t *status,
-                            cudaStream_t st);
+                            float *y, int64_t in_f, int64_t n_ff, int n_used, int n_pairs, int tokens, int num_sms,
+                            uint32_t *status, uint64_t limit_ns, cudaStream_t st);
 
 // Tensor-core GEMM for n > QMM_GEMV_MAX_N.  x16 is the f16 workspace (packed
 // formats only).  status: the handle's device status word.

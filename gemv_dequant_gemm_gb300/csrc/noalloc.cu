@@ -87,28 +87,26 @@ extern "C" int qmm_gemm_noalloc(qmm_dtype t, const void *w, const float *x, floa
     if (st != QMM_OK) return st;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
 
-    cudaError_t e;
+    uint32_t *status = reinterpret_cast<uint32_t *>(s->scratch);
+    cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), cs);  // the status word starts each call cleared
+    if (e != cudaSuccess) return QMM_ERR_CUDA;
     if (!tensor_core) {
-        e = qmm::launch_gemv(t, w, rb, x, dst, m, k, static_cast<int>(n), s->num_sms, cs);
+        e = qmm::launch_gemv(t, w, rb, x, dst, m, k, static_cast<int>(n), s->num_sms, status, 2000000000ull, cs);
     } else {
-        uint32_t *status = reinterpret_cast<uint32_t *>(s->scratch);
-        e = cudaMemsetAsync(status, 0, sizeof(uint32_t), cs);  // the shared status word starts each call cleared
-        if (e == cudaSuccess) {
-            qmm::GemmArgs a;
-            a.dtype = t;
-            a.w = w;
-            a.rb = rb;
-            a.x = x;
-            a.dst = dst;
-            a.m = m;
-            a.k = k;
-            a.n = n;
-            a.x16 = s->scratch + kStatusBytes;
-            a.status = status;
-            a.wait_limit_ns = 2000000000ull;
-            a.debug_skip_first_b_load = 0;
-            e = qmm::launch_gemm_tc(a, s->num_sms, cs);
-        }
+        qmm::GemmArgs a;
+        a.dtype = t;
+        a.w = w;
+        a.rb = rb;
+        a.x = x;
+        a.dst = dst;
+        a.m = m;
+        a.k = k;
+        a.n = n;
+        a.x16 = s->scratch + kStatusBytes;
+        a.status = status;
+        a.wait_limit_ns = 2000000000ull;
+        a.debug_skip_first_b_load = 0;
+        e = qmm::launch_gemm_tc(a, s->num_sms, cs);
     }
     return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
 }

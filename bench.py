@@ -205,13 +205,15 @@ def run_ours(args):
 
     # ---- prefill workload: COPIES sets of (W, X, dst, workspace) ----
     gemms = []  # per GEMM: dict with host arrays and per-copy device buffers
-    for label, m, k in SHAPES:
+    copies_n = max(1, args.copies)
+    shapes = [s for s in SHAPES if not args.only or s[0] in args.only.split(",")]
+    for label, m, k in shapes:
         x_np = synth.activations(N_TOKENS, k)
         for fmt in DTYPES:
             w_np = synth.weights(fmt, m, k, m * q.qmm_row_bytes(fmt, k))
             wsb = q.qmm_gemm_workspace_bytes(fmt, m, k, N_TOKENS)
             copies = []
-            for c in range(COPIES):
+            for c in range(copies_n):
                 copies.append({
                     "w": torch.from_numpy(w_np).cuda(), "x": torch.from_numpy(x_np).cuda(),
                     "dst": torch.empty(N_TOKENS, m, dtype=torch.float32, device="cuda"),
@@ -220,6 +222,7 @@ def run_ours(args):
             gemms.append({"label": label, "fmt": fmt, "m": m, "k": k, "wsb": wsb, "w_np": w_np, "x_np": x_np,
                           "copies": copies, "flops": 2.0 * m * k * N_TOKENS})
     flops_step = sum(g["flops"] for g in gemms)
+    copy_mb = sum(b.numel() * b.element_size() for g in gemms for b in g["copies"][0].values()) / 1e6
     dt_code = {f: q.DTYPES[f] for f in DTYPES}
 
     def launch(g, c):
@@ -242,7 +245,7 @@ def run_ours(args):
     launches_per_step = sum(1 if g["fmt"] == "f32" else 2 for g in gemms)
 
     for i in range(args.warmup):
-        step(i % COPIES)
+        step(i % copies_n)
     torch.cuda.synchronize()
     if q.qmm_sync_status(h) != 0:
         raise RuntimeError("device status set during warm-up")
@@ -262,7 +265,7 @@ def run_ours(args):
         # below time kernels and not host launch gaps
         torch.cuda._sleep(1_500_000)
         ev_step[s][0].record(stream)
-        step(s % COPIES)
+        step(s % copies_n)
         ev_step[s][1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
@@ -281,7 +284,7 @@ def run_ours(args):
                  for _ in range(kb)]
     for s in range(kb):
         torch.cuda._sleep(1_500_000)
-        step(s % COPIES, ev_launch[s])
+        step(s % copies_n, ev_launch[s])
     torch.cuda.synchronize()
     launch_ms = np.array([[a.elapsed_time(b) for a, b in row] for row in ev_launch])  # [steps][gemm]
     ms_per_step = float(np.mean(step_ms))
@@ -331,7 +334,7 @@ def run_ours(args):
             torch.cuda.synchronize()
             ev0.record(stream)
             for s in range(e2e_steps):
-                c = s % COPIES
+                c = s % copies_n
                 for g, p in zip(gemms, pinned):
                     b = g["copies"][c]
                     b["w"].copy_(p["w"], non_blocking=True)
@@ -365,7 +368,7 @@ def run_ours(args):
             "data": "synthetic (seeded LCG / xorshift64 streams)",
             "config": {"workload": WORKLOAD, "n": N_TOKENS, "dtypes": DTYPES,
                        "gemms_per_step": len(gemms), "flops_per_step": flops_step,
-                       "l2": f"inputs rotated over {COPIES} copies (about {COPIES*115} MB > 129 MB L2)",
+                       "l2": f"inputs rotated over {copies_n} copies of {copy_mb:.0f} MB (L2 129 MB)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "per_dtype_tflops": per_dtype, "per_gemm": per_gemm, "roofline": roofline,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
@@ -470,6 +473,10 @@ def main(argv=None):
     ap.add_argument("--no-sub", action="store_true", help="skip the GEMV / MoE / dequant sub-benchmarks")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--only", default=None,
+                    help="comma-separated shape labels to keep (profiling runs; not a headline workload)")
+    ap.add_argument("--copies", type=int, default=COPIES,
+                    help="rotated input copies (profiling runs use 1 to keep the device footprint small)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

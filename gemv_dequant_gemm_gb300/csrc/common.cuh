@@ -33,7 +33,7 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
 
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t)::"memory");
     return t;
 }
 
@@ -71,12 +71,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // Wait until the barrier's phase with this parity has completed.  Gives up
 // when *abort becomes nonzero (another role gave up) or after limit_ns of
 // wall time; on the time limit it latches kDevTimeout in *status, raises
-// *abort and returns false.  Never traps.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                                  uint32_t *status, uint64_t limit_ns) {
-    // short waits never touch the (slow) global timer
-    for (int spin = 0; spin < 64; ++spin)
-        if (mbar_try_wait(bar, parity)) return true;
+// *abort and returns false.  Never traps.  The common case -- the phase has
+// already completed -- is one try_wait inline; the polling loop lives out of
+// line (a long inlined loop next to tcgen05.mma issue slowed the issuing
+// thread several-fold).
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                                   uint32_t *status, uint64_t limit_ns) {
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -87,6 +87,12 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
             return false;
         }
     }
+}
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                                  uint32_t *status, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, abort, status, limit_ns);
 }
 
 // Programmatic dependent launch: every kernel of the library is launched with
@@ -162,6 +168,19 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, f16 inputs, f32 accumulate.  A holds
+// row i of the M x 16 slice in TMEM lane i, two f16 per 32-bit column in k
+// order (lower half first), 8 columns from a_tmem.
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // The same with tf32 inputs taken from f32 operands in shared memory.
 __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate) {
@@ -197,6 +216,19 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// 16 registers per thread into 16 consecutive 32-bit TMEM columns of the
+// thread's lane (32 lanes from taddr's lane field).
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // Shared-memory matrix descriptor of a K-major operand in the 128-byte
 // swizzle layout: rows of 128 bytes, 8-row atoms of 1024 bytes (the stride
 // byte offset), start address in 16-byte units, descriptor version 1,
@@ -222,10 +254,10 @@ __host__ __device__ constexpr uint32_t mma_idesc(uint32_t ab_format, uint32_t m,
 }
 
 // Launch `kernel` on `st` with programmatic dependent launch allowed (and an
-// optional cluster shape).
+// optional cluster shape; 1 x 1 x 1 launches without clusters).
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                              unsigned cluster_z, Args... args) {
+                              dim3 cluster, Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -236,11 +268,11 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attrs[na].val.programmaticStreamSerializationAllowed = 1;
     ++na;
-    if (cluster_z > 1) {
+    if (cluster.x * cluster.y * cluster.z > 1) {
         attrs[na].id = cudaLaunchAttributeClusterDimension;
-        attrs[na].val.clusterDim.x = 1;
-        attrs[na].val.clusterDim.y = 1;
-        attrs[na].val.clusterDim.z = cluster_z;
+        attrs[na].val.clusterDim.x = cluster.x;
+        attrs[na].val.clusterDim.y = cluster.y;
+        attrs[na].val.clusterDim.z = cluster.z;
         ++na;
     }
     cfg.attrs = attrs;

@@ -51,9 +51,9 @@ static cudaError_t launch_dequant_t(const void *w, float *out, int64_t m, int64_
     const int64_t want = (total + 255) / 256;
     const int grid = static_cast<int>(want < 8LL * num_sms ? want : 8LL * num_sms);
     if (total < (1LL << 31) && m * k < (1LL << 31))
-        return launch_pdl(dequant_kernel<F, uint32_t>, dim3(grid), dim3(256), 0, st, 1u, static_cast<const uint8_t *>(w),
+        return launch_pdl(dequant_kernel<F, uint32_t>, dim3(grid), dim3(256), 0, st, dim3(1, 1, 1), static_cast<const uint8_t *>(w),
                           out, static_cast<uint32_t>(m), static_cast<uint32_t>(k), static_cast<uint32_t>(rb), ts);
-    return launch_pdl(dequant_kernel<F, int64_t>, dim3(grid), dim3(256), 0, st, 1u, static_cast<const uint8_t *>(w), out,
+    return launch_pdl(dequant_kernel<F, int64_t>, dim3(grid), dim3(256), 0, st, dim3(1, 1, 1), static_cast<const uint8_t *>(w), out,
                       m, k, rb, ts);
 }
 
@@ -64,7 +64,7 @@ cudaError_t launch_dequant(int dtype, const void *w, float *out, int64_t m, int6
         const int64_t n = m * k;
         const int64_t want = (n / 4 + 255) / 256 + 1;
         const int grid = static_cast<int>(want < 8LL * num_sms ? want : 8LL * num_sms);
-        return launch_pdl(copy_f32_kernel, dim3(grid), dim3(256), 0, st, 1u, static_cast<const float *>(w), out, n);
+        return launch_pdl(copy_f32_kernel, dim3(grid), dim3(256), 0, st, dim3(1, 1, 1), static_cast<const float *>(w), out, n);
     }
     case QMM_Q4_0: return launch_dequant_t<QMM_Q4_0>(w, out, m, k, rb, ts, num_sms, st);
     case QMM_Q8_0: return launch_dequant_t<QMM_Q8_0>(w, out, m, k, rb, ts, num_sms, st);

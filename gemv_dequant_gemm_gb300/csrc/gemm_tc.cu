@@ -12,27 +12,36 @@
 //               (G rows when G*row_bytes is a multiple of 16), else per-row
 //               1-D bulk copies of 16-byte aligned supersets of each row;
 //   warp 1      TMEM allocation and the single MMA-issuing thread:
-//               tcgen05.mma.kind::f16, M=128, N=BN, K=16, four per 64-wide k
-//               stage, fp32 accumulators in BN TMEM columns; tcgen05.commit
-//               releases the stages it read;
-//   warp 2      X producer: 2-D TMA of the f16 copy of X ([BN x 64] tiles,
-//               128-byte swizzle) -- X is rounded once to f16 (round to
-//               nearest even) by x_to_f16_kernel, like the cvt.rn.f16.f32
-//               converter of aprender-serve cublas_prefill/mod.rs;
-//   warps 3-10  decode: each thread turns 32 weights of one row (raw stage in
-//               shared memory) into f16 and stores them in the swizzled
-//               K-major layout the MMA reads -- no decoded weight copy ever
-//               reaches HBM; then the same warps run the epilogue.
+//               tcgen05.mma.kind::f16, M=128, N=BN, K=16, sixteen per 256-wide
+//               k stage, A (decoded W) read from tensor memory, B (X) from
+//               shared memory, fp32 accumulators in BN TMEM columns;
+//               tcgen05.commit releases the stages it read;
+//   warp 2      X producer: 2-D TMA of the f16 copy of X ([BN x 64] boxes,
+//               128-byte swizzle, four per stage) -- X is rounded once to f16
+//               (round to nearest even) by x_to_f16_kernel, like the
+//               cvt.rn.f16.f32 converter of aprender-serve cublas_prefill/mod.rs;
+//   warps 3-10  decode: thread = one W row = one TMEM lane (a warp owns the
+//               lane quarter warp%4); the two warps of a quarter take the two
+//               128-wide halves of every 256-wide k stage, turn the row's raw
+//               bytes (raw stage in shared memory) into f16 and write them
+//               into a ring of three A slots in tensor memory with tcgen05.st.
+//               The decoded weights never touch shared memory or HBM, so the
+//               shared-memory bandwidth is left to the X stream and the raw
+//               bytes; then the same warps run the epilogue.
+//
+// Stages are long on purpose: the issuing thread waits on mbarriers between
+// stages, and a wait that follows tcgen05.commit costs a few hundred cycles,
+// which sixteen queued MMAs (about a thousand cycles of tensor work) hide.
 //
 // f32 weights skip the decode: warp 2 loads W and X tiles as f32 with TMA and
-// the MMA runs kind::tf32 (K=8, four per 32-wide stage).
+// the MMA runs kind::tf32 (K=8, eight per 64-wide stage).
 //
 // Split-K: when the output has fewer tiles than the GPU has SMs, S CTAs of a
 // thread-block cluster (dims 1 x 1 x S) share one output tile, each taking a
-// contiguous share of the 256-wide k units.  Each writes its fp32 partial
-// tile to its own shared memory; after a cluster barrier CTA z sums column
-// slice z of all S partials through distributed shared memory in the fixed
-// order 0..S-1 and stores it.  No atomics: the result is deterministic.
+// contiguous share of the 256-wide k units.  Each writes its fp32 partial tile to its own shared
+// memory; after a cluster barrier CTA z sums column slice z of all S partials
+// through distributed shared memory in the fixed order 0..S-1 and stores it.
+// No atomics: the result is deterministic.
 //
 // Every mbarrier wait is bounded by a wall-clock limit; a wait that runs out
 // latches a status bit, the CTA stops issuing work, waits for its own copies
@@ -48,12 +57,10 @@ namespace qmm {
 
 namespace gemm {
 constexpr int BM = 128;
-constexpr int ROWB = 128;            // bytes of one operand row in one k stage
-constexpr int A_STAGE = BM * ROWB;   // 16 KB
+constexpr int ATOM_ROW = 128;        // bytes of one operand row in one 128-byte swizzle atom
 constexpr int RK = 256;              // k per raw-weight stage and per split-K unit
 constexpr int NUM_DECODE_WARPS = 8;
-constexpr int DEC_GROUPS = 4;        // decode warp groups; group g decodes every 4th k stage into A slot g
-constexpr int DEC_GROUP_WARPS = NUM_DECODE_WARPS / DEC_GROUPS;
+constexpr int TMEM_MAX = 512;        // TMEM columns per SM
 constexpr int WARP_RAW = 0, WARP_MMA = 1, WARP_X = 2, WARP_DEC0 = 3;
 constexpr int THREADS = 32 * (WARP_DEC0 + NUM_DECODE_WARPS);  // 352
 constexpr int MAX_SPLIT = 8;
@@ -73,8 +80,17 @@ struct Ctl {
 template <int F, int BN> struct Plan {
     static constexpr bool TF32 = (F == QMM_F32);
     static constexpr int QK = Fmt<F>::QK, BB = Fmt<F>::BB;
-    static constexpr int KPS = TF32 ? 32 : 64;           // k per MMA stage
-    static constexpr int B_STAGE = BN * ROWB;
+    // k per MMA stage: packed W takes a whole 256-wide raw unit (16 MMAs of
+    // K=16); f32 W takes 64 (8 MMAs of K=8)
+    static constexpr int KPS = TF32 ? 64 : RK;
+    static constexpr int ELEM = TF32 ? 4 : 2;
+    static constexpr int ATOMS = KPS * ELEM / ATOM_ROW;   // swizzle atoms along k per stage
+    static constexpr int KMMA = TF32 ? 8 : 16;
+    static constexpr int MMAS = KPS / KMMA;               // MMAs per stage
+    static constexpr int B_ATOM = BN * ATOM_ROW;
+    static constexpr int B_STAGE = ATOMS * B_ATOM;
+    static constexpr int A_ATOM = BM * ATOM_ROW;
+    static constexpr int A_STAGE = TF32 ? ATOMS * A_ATOM : 0;  // f32 W tiles in shared memory
     // raw stage: 256 k of every row; pitch an odd multiple of 16 bytes >= the
     // row bytes plus the largest misalignment (block rows are 2-byte aligned)
     static constexpr int RB = TF32 ? 0 : RK / QK * BB;
@@ -82,22 +98,27 @@ template <int F, int BN> struct Plan {
     static constexpr int P0 = TF32 ? 16 : (RB + SLACK + 15) / 16 * 16;
     static constexpr int P = ((P0 / 16) % 2 == 1) ? P0 : P0 + 16;
     static constexpr int RAW_STAGE = TF32 ? 0 : BM * P;
-    static constexpr int RS = TF32 ? 0 : 2;              // raw stages: 8 k stages of look-ahead
-    static constexpr int AVAIL = SMEM_LIMIT - 1024 - static_cast<int>(sizeof(Ctl)) - RS * RAW_STAGE;
-    // packed W: 4 decoded-W stages, as many X stages as fit (at most 8);
-    // f32 W: W and X tiles travel together, as many stages as fit
-    static constexpr int AS0 = TF32 ? AVAIL / (A_STAGE + B_STAGE) : DEC_GROUPS;
-    static constexpr int AS = AS0 > MAXS ? MAXS : AS0;
-    static constexpr int BS0 = TF32 ? AS : (AVAIL - AS * A_STAGE) / B_STAGE;
+    static constexpr int CTL = static_cast<int>(sizeof(Ctl));
+    // raw stages: three when that still leaves room for two X stages, else two
+    static constexpr int RS = TF32 ? 0 : ((SMEM_LIMIT - 1024 - CTL - 3 * RAW_STAGE >= 2 * B_STAGE) ? 3 : 2);
+    static constexpr int AVAIL = SMEM_LIMIT - 1024 - CTL - RS * RAW_STAGE;
+    // X (and f32 W) stages: as many as fit, at most MAXS
+    static constexpr int BS0 = AVAIL / (B_STAGE + A_STAGE);
     static constexpr int BS = BS0 > MAXS ? MAXS : BS0;
-    static constexpr int FIXED = BS * B_STAGE + AS * A_STAGE;
-    static constexpr int RING = FIXED + RS * RAW_STAGE;
+    // decoded-W (A) stages: packed W in tensor memory after the accumulator
+    // (KPS/2 columns each: two f16 per column); f32 W with the X stages
+    static constexpr int A_COLS = KPS / 2;
+    static constexpr int AS0 = TF32 ? BS : (TMEM_MAX - BN) / A_COLS;
+    static constexpr int AS = AS0 > MAXS ? MAXS : AS0;
+    static constexpr int RING = BS * (B_STAGE + A_STAGE) + RS * RAW_STAGE;
+    static constexpr int TMEM_COLS = TF32 ? BN : TMEM_MAX;
     static constexpr int RED = BM * BN * 4;               // split-K partial tile (aliases the rings)
     static constexpr int BODY = RING > RED ? RING : RED;
     static constexpr size_t SMEM = 1024 + BODY + sizeof(Ctl);
     static_assert(TF32 || RS >= 2, "raw ring needs two stages");
     static_assert(BS >= 2 && AS >= 2, "rings need two stages");
-    static_assert(TF32 || AS == DEC_GROUPS, "one decoded-W slot per decode group");
+    static_assert(TF32 || BN + AS * A_COLS <= TMEM_MAX, "A slots exceed tensor memory");
+    static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0 && TMEM_COLS >= 32 && TMEM_COLS <= 512, "TMEM allocation");
     static_assert(SMEM <= SMEM_LIMIT, "shared memory plan too large");
     static constexpr uint32_t IDESC = mma_idesc(TF32 ? 2u : 0u, BM, BN);
 };
@@ -147,8 +168,8 @@ struct GemmParams {
     float *dst;
     int M, N, K;
     int units;   // 256-wide k units: ceil(K / 256)
-    int raw_g;   // rows per 16-byte-aligned row group of the raw-weight tensor map; 0 = per-row bulk copies
     int w_early; // 1: the kernel before this one only wrote the f16 copy of X, so W may be read before it ends
+    int raw_g;   // rows per 16-byte-aligned row group of the raw-weight tensor map; 0 = per-row bulk copies
     int splits;  // CTAs per output tile (cluster size along z)
     uint32_t *status;
     uint64_t limit_ns;
@@ -168,8 +189,8 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sB = base;
-    uint8_t *sA = sB + BS * PL::B_STAGE;
-    uint8_t *sRaw = sA + AS * A_STAGE;
+    uint8_t *sA = sB + BS * PL::B_STAGE;  // f32 W only
+    uint8_t *sRaw = sA + BS * PL::A_STAGE;
     float *sRed = reinterpret_cast<float *>(base);  // split-K partial, after the main loop
     Ctl *ctl = reinterpret_cast<Ctl *>(base + PL::BODY);
 
@@ -187,7 +208,7 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
         for (int s = 0; s < MAXS; ++s) {
             mbar_init(&ctl->b_full[s], 1);
             mbar_init(&ctl->b_empty[s], 1);
-            mbar_init(&ctl->a_full[s], DEC_GROUP_WARPS);
+            mbar_init(&ctl->a_full[s], NUM_DECODE_WARPS);
             mbar_init(&ctl->a_empty[s], 1);
             mbar_init(&ctl->raw_full[s], 1);
             mbar_init(&ctl->raw_empty[s], NUM_DECODE_WARPS);
@@ -200,7 +221,7 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
         if (!TF32 && p.raw_g > 0) prefetch_tensormap(&tmap_raw);
     }
     if (warp == WARP_MMA) {
-        tmem_alloc(&ctl->tmem_base, BN);
+        tmem_alloc(&ctl->tmem_base, PL::TMEM_COLS);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -225,13 +246,13 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
                 const bool ok = mbar_wait_bounded(&ctl->raw_empty[r], ph ^ 1, abort, p.status, p.limit_ns);
                 if (!__all_sync(0xFFFFFFFFu, ok)) break;
                 const int64_t seg_off = static_cast<int64_t>(u) * PL::RB;
+                uint8_t *stage = sRaw + r * PL::RAW_STAGE;
                 if (p.raw_g > 0) {
                     // one 2-D TMA box per row residue g: rows m0+g, m0+g+G, ... land
                     // contiguously at slots g*(BM/G) ... with pitch P
                     if (lane == 0) {
                         const int G = p.raw_g;
                         mbar_arrive_expect_tx(&ctl->raw_full[r], BM * PL::P);
-                        uint8_t *stage = sRaw + r * PL::RAW_STAGE;
                         for (int g = 0; g < G; ++g) {
                             const int64_t xb = (static_cast<int64_t>(g) * p.rb + seg_off) & ~int64_t(15);
                             tma_load_2d(stage + g * (BM / G) * PL::P, &tmap_raw, static_cast<int32_t>(xb / 2), m0 / G,
@@ -264,7 +285,6 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
                 for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xFFFFFFFFu, tot, o);
                 if (lane == 0) mbar_arrive_expect_tx(&ctl->raw_full[r], tot);
                 __syncwarp();
-                uint8_t *stage = sRaw + r * PL::RAW_STAGE;
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                     if (bytes[j]) bulk_load_1d(stage + (lane + 32 * j) * PL::P, src[j], bytes[j], &ctl->raw_full[r]);
@@ -287,13 +307,13 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
                 const uint32_t ph = (i / BS) & 1;
                 if (!mbar_wait_bounded(&ctl->b_empty[s], ph ^ 1, abort, p.status, p.limit_ns)) break;
                 if (p.debug_skip && i == 0) continue;  // test hook: stage 0 never fills
-                if constexpr (TF32) {
-                    mbar_arrive_expect_tx(&ctl->b_full[s], A_STAGE + PL::B_STAGE);
-                    tma_load_2d(sA + s * A_STAGE, &tmap_w, kt * KPS, m0, &ctl->b_full[s]);
-                } else {
-                    mbar_arrive_expect_tx(&ctl->b_full[s], PL::B_STAGE);
+                mbar_arrive_expect_tx(&ctl->b_full[s], PL::B_STAGE + PL::A_STAGE);
+#pragma unroll
+                for (int j = 0; j < PL::ATOMS; ++j) {
+                    const int kx = kt * KPS + j * (ATOM_ROW / PL::ELEM);
+                    if constexpr (TF32) tma_load_2d(sA + s * PL::A_STAGE + j * PL::A_ATOM, &tmap_w, kx, m0, &ctl->b_full[s]);
+                    tma_load_2d(sB + s * PL::B_STAGE + j * PL::B_ATOM, &tmap_x, kx, n0, &ctl->b_full[s]);
                 }
-                tma_load_2d(sB + s * PL::B_STAGE, &tmap_x, kt * KPS, n0, &ctl->b_full[s]);
                 last[s] = i;
             }
             if (*abort) {
@@ -310,16 +330,21 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
                 if (!mbar_wait_bounded(&ctl->b_full[sb], (i / BS) & 1, abort, p.status, p.limit_ns)) break;
                 if (!TF32 && !mbar_wait_bounded(&ctl->a_full[sa], (i / AS) & 1, abort, p.status, p.limit_ns)) break;
                 tc_fence_after();
-                const uint32_t a_addr = smem_u32(sA + sa * A_STAGE);
                 const uint32_t b_addr = smem_u32(sB + sb * PL::B_STAGE);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t ad = sw128_desc(a_addr + 32 * kk);
-                    const uint64_t bd = sw128_desc(b_addr + 32 * kk);
-                    if constexpr (TF32)
+                for (int kk = 0; kk < PL::MMAS; ++kk) {
+                    // K step kk: atom kk/4, 32 bytes (16 f16 or 8 f32) per step inside the atom
+                    const uint32_t off = static_cast<uint32_t>((kk >> 2) * PL::B_ATOM + 32 * (kk & 3));
+                    const uint64_t bd = sw128_desc(b_addr + off);
+                    if constexpr (TF32) {
+                        const uint32_t aoff = static_cast<uint32_t>((kk >> 2) * PL::A_ATOM + 32 * (kk & 3));
+                        const uint64_t ad = sw128_desc(smem_u32(sA + sa * PL::A_STAGE) + aoff);
                         mma_tf32(tmem, ad, bd, PL::IDESC, (i | kk) != 0);
-                    else
-                        mma_f16(tmem, ad, bd, PL::IDESC, (i | kk) != 0);
+                    } else {
+                        // A slot sa: A_COLS columns after the accumulator, 8 per K=16 step
+                        const uint32_t at = tmem + BN + static_cast<uint32_t>(sa * PL::A_COLS + 8 * kk);
+                        mma_f16_tmem_a(tmem, at, bd, PL::IDESC, (i | kk) != 0);
+                    }
                 }
                 mma_commit(&ctl->b_empty[sb]);
                 if (!TF32) mma_commit(&ctl->a_empty[sa]);
@@ -329,63 +354,49 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
         __syncwarp();
     } else {
         // ------------- decode warps -------------
-        // Group g (two warps) decodes k stages g, g+4, g+8, ... into A slot g,
-        // so four stages are in flight and their barrier round trips overlap.
-        // Each thread turns 4 items of 32 weights (rows tg and tg+64, both
-        // 32-wide halves of the stage) into f16.
+        // Thread = W row 32*(warp%4) + lane = TMEM lane; warps 3-6 decode the
+        // first 128 k of every 256-wide stage, warps 7-10 the second.
         if constexpr (!TF32) {
-            const int dt = threadIdx.x - 32 * WARP_DEC0;
-            const int g = dt / (32 * DEC_GROUP_WARPS);
-            const int tg = dt % (32 * DEC_GROUP_WARPS);
-            uint32_t rowoff[2], misb[2];
-            int gmr[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int row = tg + 64 * h;
-                const int slot = (p.raw_g > 0) ? (row % p.raw_g) * (BM / p.raw_g) + row / p.raw_g : row;
-                rowoff[h] = static_cast<uint32_t>(slot * PL::P);
-                gmr[h] = m0 + row;
-                misb[h] = static_cast<uint32_t>(
-                    (reinterpret_cast<uintptr_t>(p.w) + static_cast<int64_t>(gmr[h] < p.M ? gmr[h] : 0) * p.rb) & 15u);
-            }
+            static_assert(KPS == RK, "one raw unit per MMA stage");
+            const int q = warp & 3;
+            const int hh = (warp - WARP_DEC0) >> 2;
+            const int row = 32 * q + lane;
+            const int slot = (p.raw_g > 0) ? (row % p.raw_g) * (BM / p.raw_g) + row / p.raw_g : row;
+            const uint32_t rowoff = static_cast<uint32_t>(slot * PL::P);
+            const int gm = m0 + row;
+            const uint32_t misb = static_cast<uint32_t>(
+                (reinterpret_cast<uintptr_t>(p.w) + static_cast<int64_t>(gm < p.M ? gm : 0) * p.rb) & 15u);
             const uint32_t raw0 = smem_u32(sRaw);
-            for (int i = g; i < NK; i += DEC_GROUPS) {
-                const int kt = kt0 + i, sa = g;
-                const int ui = kt / SPU - u0, r = ui % RS;  // raw stage of this k stage
+            const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16) + BN + 64u * hh;
+            for (int i = 0; i < NK; ++i) {
+                const int kt = kt0 + i, sa = i % AS, r = i % RS;
                 {
-                    const bool ok = mbar_wait_bounded(&ctl->raw_full[r], (ui / RS) & 1, abort, p.status, p.limit_ns);
+                    const bool ok = mbar_wait_bounded(&ctl->raw_full[r], (i / RS) & 1, abort, p.status, p.limit_ns);
                     if (!__all_sync(0xFFFFFFFFu, ok)) break;
                 }
                 const bool ok = mbar_wait_bounded(&ctl->a_empty[sa], ((i / AS) & 1) ^ 1, abort, p.status, p.limit_ns);
                 if (!__all_sync(0xFFFFFFFFu, ok)) break;
-                const uint32_t useg = static_cast<uint32_t>((kt / SPU) * PL::RB);
-                const uint32_t rawst = raw0 + static_cast<uint32_t>(r * PL::RAW_STAGE);
-                uint8_t *abase = sA + sa * A_STAGE;
+                tc_fence_after();
+                const uint32_t mis = (misb + static_cast<uint32_t>(kt * PL::RB)) & 15u;
+                const uint32_t src = raw0 + static_cast<uint32_t>(r * PL::RAW_STAGE) + rowoff + mis;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int h = j & 1, half = j >> 1;
-                    const int row = tg + 64 * h;
+                for (int t = 0; t < 4; ++t) {
+                    const int e0 = 128 * hh + 32 * t;  // within the 256-wide unit
                     uint32_t o[16];
-                    if (gmr[h] < p.M && static_cast<int64_t>(kt) * 64 + half * 32 < p.K) {
-                        const uint32_t mis = (misb[h] + useg) & 15u;
-                        decode32_s<F>(rawst + rowoff[h] + mis, (kt % SPU) * 64 + half * 32, o);
+                    if (gm < p.M && static_cast<int64_t>(kt) * RK + e0 < p.K) {
+                        decode32_s<F>(src, e0, o);
                     } else {
 #pragma unroll
                         for (int q2 = 0; q2 < 16; ++q2) o[q2] = 0u;
                     }
-                    uint8_t *rowp = abase + (row >> 3) * 1024 + (row & 7) * 128;
-#pragma unroll
-                    for (int q2 = 0; q2 < 4; ++q2) {
-                        const int c = half * 4 + q2;
-                        *reinterpret_cast<uint4 *>(rowp + ((c ^ (row & 7)) << 4)) =
-                            make_uint4(o[4 * q2], o[4 * q2 + 1], o[4 * q2 + 2], o[4 * q2 + 3]);
-                    }
+                    tmem_st_32x32b_x16(tq + static_cast<uint32_t>(sa * PL::A_COLS + 16 * t), o);
                 }
-                fence_proxy_async_smem();
+                tmem_st_wait();
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&ctl->a_full[sa]);
-                    mbar_arrive(&ctl->raw_empty[r]);  // every group takes one stage of each raw stage
+                    mbar_arrive(&ctl->raw_empty[r]);
                 }
             }
         }
@@ -471,7 +482,7 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
     __syncthreads();
     if (warp == WARP_MMA) {
         tc_fence_after();
-        tmem_dealloc(tmem, BN);
+        tmem_dealloc(tmem, PL::TMEM_COLS);
     }
 }
 
@@ -588,7 +599,7 @@ static cudaError_t launch_gemm_t(const GemmArgs &a, int num_sms, cudaStream_t st
         const int64_t total8 = a.n * a.k / 8;
         const int64_t want = (total8 + 255) / 256;
         const int grid = static_cast<int>(want < 8LL * num_sms ? want : 8LL * num_sms);
-        cudaError_t e = launch_pdl(x_to_f16_kernel, dim3(grid), dim3(256), 0, st, 1u, a.x,
+        cudaError_t e = launch_pdl(x_to_f16_kernel, dim3(grid), dim3(256), 0, st, dim3(1, 1, 1), a.x,
                                    static_cast<__half *>(a.x16), total8);
         if (e != cudaSuccess) return e;
         if (!make_map(&map_x, a.x16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.n, a.k, BN, 64)) return cudaErrorInvalidValue;
@@ -606,15 +617,15 @@ static cudaError_t launch_gemm_t(const GemmArgs &a, int num_sms, cudaStream_t st
     p.units = static_cast<int>((a.k + RK - 1) / RK);
     p.raw_g = raw_g;
     p.w_early = pdl ? 1 : 0;
-    const int64_t tiles = ((a.m + BM - 1) / BM) * ((a.n + BN - 1) / BN);
-    p.splits = choose_splits(tiles, p.units, num_sms);
+    const int64_t m_tiles = (a.m + BM - 1) / BM, n_tiles = (a.n + BN - 1) / BN;
+    p.splits = choose_splits(m_tiles * n_tiles, p.units, num_sms);
     p.status = a.status;
     p.limit_ns = a.wait_limit_ns;
     p.debug_skip = a.debug_skip_first_b_load;
 
-    const dim3 grid(static_cast<unsigned>((a.m + BM - 1) / BM), static_cast<unsigned>((a.n + BN - 1) / BN),
-                    static_cast<unsigned>(p.splits));
-    return launch_pdl(gemm_tc_kernel<F, BN>, grid, dim3(THREADS), PL::SMEM, st, static_cast<unsigned>(p.splits),
+    const dim3 grid(static_cast<unsigned>(m_tiles), static_cast<unsigned>(n_tiles), static_cast<unsigned>(p.splits));
+    const dim3 cluster(1, 1, static_cast<unsigned>(p.splits));
+    return launch_pdl(gemm_tc_kernel<F, BN>, grid, dim3(THREADS), PL::SMEM, st, cluster,
                       map_x, map_w, map_raw, p);
 }
 

@@ -499,7 +499,7 @@ static cudaError_t launch_gemv_nv(const gv::Params &p, int num_sms, cudaStream_t
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int grid = std::min(p.total_stages, num_sms * gemv_ctas_per_sm<NV>());
-    return launch_pdl(gemv_kernel<F, NV>, dim3(grid), dim3(THREADS), smem, st, 1u, p);
+    return launch_pdl(gemv_kernel<F, NV>, dim3(grid), dim3(THREADS), smem, st, dim3(1, 1, 1), p);
 }
 
 template <int F>

@@ -457,6 +457,406 @@ __global__ void __launch_bounds__(gv::THREADS, gemv_ctas_per_sm<NV>()) gemv_kern
 }
 
 // ---------------------------------------------------------------------------
+// Register-X GEMV: for small n the X values each thread needs stay in its
+// registers for the whole launch, so per weight only the packed bytes are read
+// from shared memory.  A thread owns fixed k slices ("units" of UW weights,
+// one scale region of NVFP4 or 8 weights otherwise): unit u = tk + TK*j of
+// every row, j < J, where tk is the thread's index in its k team of TK
+// threads.  The 256 compute threads form 256/TK teams; a stage holds
+// teams*RT rows, team t taking rows t*RT .. t*RT+RT-1.  Rows are handled in
+// groups of four: each warp reduces the group's 4*NVP sums (NVP = n rounded
+// up to a power of two) across its lanes with a butterfly that leaves value
+// i in lane i, and writes them to a per-warp partial buffer.  The producer
+// warp, when the stage's slot comes back to it, adds the partials of a
+// team's warps in warp order and stores the results.
+// ---------------------------------------------------------------------------
+namespace gr {
+constexpr int COMPUTE_WARPS = 16;
+constexpr int THREADS = 32 * (COMPUTE_WARPS + 1);
+constexpr int NT = 32 * COMPUTE_WARPS;  // compute threads
+constexpr int MAX_RING = 8;
+constexpr int XREG = 32;                // X floats one thread holds
+constexpr int PART = 32;                // partial sums per warp and stage
+constexpr int MAX_TABLE = 256;
+constexpr int SMEM_BUDGET = 226 * 1024;
+
+struct Params {
+    const uint8_t *w;
+    const void *const *w_ptrs;
+    const float *scales;
+    const float *x;
+    float *dst;
+    int64_t k, rb;
+    int rows_per_mat, mats, n_pairs, n_used, tokens;
+    int tk, J, rt, teams, stage_rows;
+    int stages_per_mat, total_stages, stage_bytes, ring;
+    uint32_t *status;
+    uint64_t limit_ns;
+};
+
+struct Ctl {
+    uint64_t full[MAX_RING], empty[MAX_RING];
+    const uint8_t *mptr[MAX_TABLE];
+    float mscale[MAX_TABLE];
+    int bad[MAX_RING];
+    int abort;
+    int pad;
+};
+
+template <int F> struct Unit { static constexpr int W = (F == QMM_NVFP4) ? 16 : 8; };
+template <int NV> constexpr int nv_pow2() { return NV <= 1 ? 1 : (NV <= 2 ? 2 : (NV <= 4 ? 4 : 8)); }
+template <int F, int NV> constexpr int jmax() {
+    return XREG / (NV * Unit<F>::W) >= 1 ? XREG / (NV * Unit<F>::W) : 1;
+}
+}  // namespace gr
+
+// Units of UW weights: values v (exact small numbers), scale, Q4_K offset.
+template <int F, int UW> struct UnitDec;
+template <int F> struct UnitDec<F, 8> {
+    static __device__ __forceinline__ void run(const uint8_t *row, int64_t e0, int64_t k, float (&v)[8], float &scale,
+                                               float &offset) {
+        Grp g;
+        grp8<F>(row, e0, k, g);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = g.v[j];
+        scale = g.scale;
+        offset = g.offset;
+    }
+};
+// NVFP4: 16 weights of one scale region (e0 % 16 == 0): v = 2 * e2m1 value,
+// scale = e4m3 / 2.
+template <> struct UnitDec<QMM_NVFP4, 16> {
+    static __device__ __forceinline__ void run(const uint8_t *row, int64_t e0, int64_t, float (&v)[16], float &scale,
+                                               float &offset) {
+        const uint8_t *blk = row + (e0 >> 6) * 36;
+        const int e = static_cast<int>(e0 & 63);
+        scale = 0.5f * e4m3_to_f32(LdS::u8(blk + (e >> 4)));
+        offset = 0.0f;
+        const uint32_t c0 = LdS::u32(blk + 4 + (e >> 1)), c1 = LdS::u32(blk + 8 + (e >> 1));
+        const uint32_t b[4] = {e2m1x4_offset_bytes(c0), e2m1x4_offset_bytes(c0 >> 16), e2m1x4_offset_bytes(c1),
+                               e2m1x4_offset_bytes(c1 >> 16)};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[4 * q + j] = byte_as_float(b[q], j, 8388620.0f);
+    }
+};
+
+// Packed pairs of f32 (Blackwell f32x2 arithmetic: two independent
+// round-to-nearest operations per instruction, same results as scalar ones).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t lds8(uint32_t a) {
+    uint16_t v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+
+// 16 NVFP4 weights of one scale region (codes at shared address `codes`,
+// scale byte at `scb`) as 8 f32 pairs holding twice the e2m1 values: the bytes
+// 2*value + 12 become (2^23 + byte) by byte permutation and one f32x2
+// subtraction leaves 2*value exactly.  *scale receives the e4m3 scale.
+__device__ __forceinline__ void nvfp4_unit16(uint32_t codes, uint32_t scb, uint64_t (&w2)[8], float &scale) {
+    const uint32_t c0 = lds32(codes), c1 = lds32(codes + 4);
+    scale = e4m3_to_f32(lds8(scb));
+    const uint32_t n0 = c0 ^ 0x88888888u, n1 = c1 ^ 0x88888888u;
+    const uint32_t b[4] = {
+        prmt_signed(0x0F0E0D0Cu, 0x18141210u, c0) | prmt_signed(0x090A0B0Cu, 0x00040608u, n0),
+        prmt_signed(0x0F0E0D0Cu, 0x18141210u, c0 >> 16) | prmt_signed(0x090A0B0Cu, 0x00040608u, n0 >> 16),
+        prmt_signed(0x0F0E0D0Cu, 0x18141210u, c1) | prmt_signed(0x090A0B0Cu, 0x00040608u, n1),
+        prmt_signed(0x0F0E0D0Cu, 0x18141210u, c1 >> 16) | prmt_signed(0x090A0B0Cu, 0x00040608u, n1 >> 16)};
+    const uint64_t minus = f2_pack(-8388620.0f, -8388620.0f);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        w2[2 * q] = f2_add(f2_pack(__uint_as_float(__byte_perm(b[q], 0x4B000000u, 0x7440u)),
+                                   __uint_as_float(__byte_perm(b[q], 0x4B000000u, 0x7441u))), minus);
+        w2[2 * q + 1] = f2_add(f2_pack(__uint_as_float(__byte_perm(b[q], 0x4B000000u, 0x7442u)),
+                                       __uint_as_float(__byte_perm(b[q], 0x4B000000u, 0x7443u))), minus);
+    }
+}
+
+// sum_i w2[i] . x2[i] over 8 pairs, two f32x2 chains.
+__device__ __forceinline__ float dot16_f2(const uint64_t (&w2)[8], const uint64_t (&x2)[8]) {
+    uint64_t a0 = f2_fma(w2[0], x2[0], f2_pack(0.0f, 0.0f));
+    uint64_t a1 = f2_fma(w2[1], x2[1], f2_pack(0.0f, 0.0f));
+#pragma unroll
+    for (int q = 1; q < 4; ++q) {
+        a0 = f2_fma(w2[2 * q], x2[2 * q], a0);
+        a1 = f2_fma(w2[2 * q + 1], x2[2 * q + 1], a1);
+    }
+    const float2 s0 = f2_unpack(a0), s1 = f2_unpack(a1);
+    return (s0.x + s0.y) + (s1.x + s1.y);
+}
+
+// UW consecutive X values of one activation row (zero past k).
+template <int UW> __device__ __forceinline__ void load_xu(const float *xr, int64_t e0, int64_t k, float (&v)[UW]) {
+    if (e0 + UW <= k && (k % 4) == 0) {
+#pragma unroll
+        for (int q = 0; q < UW / 4; ++q) {
+            const float4 a = __ldg(reinterpret_cast<const float4 *>(xr + e0) + q);
+            v[4 * q] = a.x;
+            v[4 * q + 1] = a.y;
+            v[4 * q + 2] = a.z;
+            v[4 * q + 3] = a.w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < UW; ++j) v[j] = (e0 + j < k) ? __ldg(xr + e0 + j) : 0.0f;
+    }
+}
+
+// Butterfly reduction of V values (a power of two <= 32) over the warp:
+// afterwards lane l holds the warp total of value l % V in a[0].
+template <int V> __device__ __forceinline__ float warp_transpose_sum(float (&a)[V], int lane) {
+#pragma unroll
+    for (int h = V / 2; h >= 1; h >>= 1) {
+        const bool upper = (lane & h) != 0;
+#pragma unroll
+        for (int t = 0; t < h; ++t) {
+            const float send = upper ? a[t] : a[t + h];
+            const float keep = upper ? a[t + h] : a[t];
+            a[t] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, h);
+        }
+    }
+#pragma unroll
+    for (int off = V; off < 32; off <<= 1) a[0] += __shfl_xor_sync(0xFFFFFFFFu, a[0], off);
+    return a[0];
+}
+
+template <int F, int NV, int JM>
+__global__ void __launch_bounds__(gr::THREADS, 1) gemv_rx_kernel(const gr::Params p) {
+    using namespace gr;
+    constexpr int UW = Unit<F>::W;
+    constexpr int NVP = nv_pow2<NV>();
+    constexpr int RG = 4;            // rows per group
+    constexpr int V = RG * NVP;      // values reduced per group
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    float *partial = reinterpret_cast<float *>(ring + p.ring * p.stage_bytes);  // [ring][8 warps][PART]
+    Ctl *ctl = reinterpret_cast<Ctl *>(partial + p.ring * COMPUTE_WARPS * PART);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < MAX_RING; ++s) {
+            mbar_init(&ctl->full[s], 1);
+            mbar_init(&ctl->empty[s], COMPUTE_WARPS);
+            ctl->bad[s] = 0;
+        }
+        ctl->abort = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    griddep_wait();
+    if (threadIdx.x == 0) griddep_launch();
+    volatile int *abort = &ctl->abort;
+    const bool moe = p.w_ptrs != nullptr;
+    const int s_begin = static_cast<int>(static_cast<int64_t>(blockIdx.x) * p.total_stages / gridDim.x);
+    const int s_end = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * p.total_stages / gridDim.x);
+    const int nst = s_end - s_begin;
+    const bool table = moe && p.mats <= MAX_TABLE;
+    if (table) {
+        for (int i = threadIdx.x; i < p.mats; i += THREADS) {
+            ctl->mptr[i] = static_cast<const uint8_t *>(p.w_ptrs[i]);
+            ctl->mscale[i] = __ldg(p.scales + i);
+        }
+    }
+    __syncthreads();
+    const int nunits = static_cast<int>((p.k + UW - 1) / UW);
+    const float nan = __int_as_float(0x7FC00000);
+
+    if (warp == COMPUTE_WARPS) {
+        // ---------------- producer: stage loads and the cross-warp sums ----------------
+        const int wpt = p.tk / 32;  // warps per team
+        int issued = 0;
+        for (int j = 0; j < nst + p.ring; ++j) {
+            const int slot = j % p.ring;
+            if (j >= p.ring || j >= nst) {
+                // the stage that used this slot, jr, has been consumed by every compute warp
+                const int jr = j - p.ring;
+                if (jr >= 0) {
+                    const bool ok = mbar_wait_bounded(&ctl->empty[slot], (jr / p.ring) & 1, abort, p.status, p.limit_ns);
+                    if (!__all_sync(0xFFFFFFFFu, ok)) break;
+                    const int s = s_begin + jr;
+                    const int mat = s / p.stages_per_mat;
+                    const int r0 = (s % p.stages_per_mat) * p.stage_rows;
+                    const int rows = min(p.stage_rows, p.rows_per_mat - r0);
+                    const bool bad = ctl->bad[slot] != 0;
+                    const float scale = !moe ? 1.0f : (table ? ctl->mscale[mat] : __ldg(p.scales + mat));
+                    const float *pb = partial + slot * COMPUTE_WARPS * PART;
+                    for (int o = lane; o < rows * NV; o += 32) {
+                        const int rl = o / NV, v = o % NV;
+                        const int tm = rl / p.rt, i = rl % p.rt;
+                        float sum = 0.0f;
+                        for (int w = 0; w < wpt; ++w) sum += pb[(tm * wpt + w) * PART + i * NVP + v];
+                        const float val = bad ? nan : scale * sum;
+                        if (moe)
+                            p.dst[static_cast<int64_t>(mat) * p.rows_per_mat + r0 + rl] = val;
+                        else
+                            p.dst[static_cast<int64_t>(v) * p.rows_per_mat + r0 + rl] = val;
+                    }
+                    if (bad && lane == 0) atomicOr(p.status, kDevBadPtr);
+                }
+            }
+            if (j < nst && lane == 0) {
+                const int s = s_begin + j;
+                const int mat = s / p.stages_per_mat;
+                const int r0 = (s % p.stages_per_mat) * p.stage_rows;
+                const int rows = min(p.stage_rows, p.rows_per_mat - r0);
+                const uint8_t *mp = !moe ? p.w : (table ? ctl->mptr[mat] : static_cast<const uint8_t *>(p.w_ptrs[mat]));
+                if (mp == nullptr || (reinterpret_cast<uintptr_t>(mp) & 15u) != 0) {
+                    ctl->bad[slot] = 1;
+                    mbar_arrive(&ctl->full[slot]);
+                } else {
+                    ctl->bad[slot] = 0;
+                    const uint8_t *src = mp + static_cast<int64_t>(r0) * p.rb;
+                    const uintptr_t a = reinterpret_cast<uintptr_t>(src) & ~uintptr_t(15);
+                    const uint32_t len = (static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src) - a) +
+                                          static_cast<uint32_t>(rows * p.rb) + 15u) & ~15u;
+                    mbar_arrive_expect_tx(&ctl->full[slot], len);
+                    bulk_load_1d(ring + slot * p.stage_bytes, reinterpret_cast<const void *>(a), len, &ctl->full[slot]);
+                }
+            }
+            if (j < nst) ++issued;
+            __syncwarp();
+        }
+        // on abort: copies still in flight land before the CTA exits
+        if (lane == 0 && *abort) {
+            for (int j = max(0, issued - p.ring); j < issued; ++j)
+                mbar_wait_drain_any(&ctl->full[j % p.ring], (j / p.ring) & 1, p.status, p.limit_ns);
+        }
+        __syncwarp();
+    } else {
+        // ---------------- compute warps ----------------
+        const int tid = threadIdx.x;
+        const int team = tid / p.tk, tk = tid % p.tk;
+        float xr[JM][NV][UW];
+        float xs[JM][NV];  // per-unit sums of X (Q4_K minimum term)
+        uint64_t x2[JM][NV][8];  // NVFP4: X pairs halved (the codes decode to twice their value)
+        uint32_t scoff[JM], cdoff[JM];  // NVFP4: byte offsets of each unit's scale and codes in a row
+        if constexpr (F == QMM_NVFP4) {
+#pragma unroll
+            for (int jj = 0; jj < JM; ++jj) {
+                const uint32_t e0 = static_cast<uint32_t>(tk + p.tk * jj) * 16u;
+                const uint32_t blk = (e0 >> 6) * 36u, e = e0 & 63u;
+                scoff[jj] = blk + (e >> 4);
+                cdoff[jj] = blk + 4u + (e >> 1);
+            }
+        }
+        int cur_tok = -1;
+        bool dead = false;
+        for (int j = 0; j < nst; ++j) {
+            const int s = s_begin + j;
+            const int slot = j % p.ring;
+            const int mat = s / p.stages_per_mat;
+            const int tok = moe ? (mat % p.n_pairs) / p.n_used : 0;
+            if (tok != cur_tok) {  // uniform over the CTA: the stage decides it
+                cur_tok = tok;
+#pragma unroll
+                for (int jj = 0; jj < JM; ++jj) {
+                    const int u = tk + p.tk * jj;  // every unit exists: the team covers k exactly
+#pragma unroll
+                    for (int v = 0; v < NV; ++v) {
+                        load_xu<UW>(p.x + static_cast<int64_t>(tok + v) * p.k, static_cast<int64_t>(u) * UW, p.k,
+                                    xr[jj][v]);
+                        float t = 0.0f;
+#pragma unroll
+                        for (int w = 0; w < UW; ++w) t += xr[jj][v][w];
+                        xs[jj][v] = t;
+                        if constexpr (F == QMM_NVFP4) {
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                x2[jj][v][q] = f2_pack(0.5f * xr[jj][v][2 * q], 0.5f * xr[jj][v][2 * q + 1]);
+                        }
+                    }
+                }
+            }
+            const bool got = dead ? false : mbar_wait_bounded(&ctl->full[slot], (j / p.ring) & 1, abort, p.status, p.limit_ns);
+            if (!__all_sync(0xFFFFFFFFu, got)) dead = true;
+            const int r0 = (s % p.stages_per_mat) * p.stage_rows;
+            const int rows = min(p.stage_rows, p.rows_per_mat - r0);
+            const bool bad = !dead && ctl->bad[slot] != 0;
+            const uint8_t *mp = !moe ? p.w : (table ? ctl->mptr[mat] : static_cast<const uint8_t *>(p.w_ptrs[mat]));
+            const uint8_t *buf = ring + slot * p.stage_bytes +
+                                 ((reinterpret_cast<uintptr_t>(mp) + static_cast<int64_t>(r0) * p.rb) & 15u);
+            float *pw = partial + (slot * COMPUTE_WARPS + warp) * PART;
+            const uint32_t sbase = smem_u32(buf);
+            // rows past the end of the matrix (last stage) are computed from
+            // stale, in-bounds stage bytes and never stored
+#pragma unroll 1
+            for (int i0 = 0; i0 < p.rt; i0 += RG) {
+                float acc[V];
+#pragma unroll
+                for (int q = 0; q < V; ++q) acc[q] = 0.0f;
+                if (!bad && !dead) {
+#pragma unroll
+                    for (int r = 0; r < RG; ++r) {
+                        const int rl = team * p.rt + i0 + r;
+                        const uint8_t *rowp = buf + static_cast<int64_t>(rl) * p.rb;
+                        const uint32_t rbase = sbase + static_cast<uint32_t>(rl) * static_cast<uint32_t>(p.rb);
+#pragma unroll
+                        for (int jj = 0; jj < JM; ++jj) {
+                            const int u = tk + p.tk * jj;
+                            if constexpr (F == QMM_NVFP4) {
+                                uint64_t w2[8];
+                                float sc;
+                                nvfp4_unit16(rbase + cdoff[jj], rbase + scoff[jj], w2, sc);
+#pragma unroll
+                                for (int v = 0; v < NV; ++v)
+                                    acc[r * NVP + v] = __fmaf_rn(sc, dot16_f2(w2, x2[jj][v]), acc[r * NVP + v]);
+                            } else {
+                                float wv[UW], sc, off;
+                                UnitDec<F, UW>::run(rowp, static_cast<int64_t>(u) * UW, p.k, wv, sc, off);
+#pragma unroll
+                                for (int v = 0; v < NV; ++v) {
+                                    float c[4];
+#pragma unroll
+                                    for (int q = 0; q < 4; ++q) c[q] = wv[q] * xr[jj][v][q];
+#pragma unroll
+                                    for (int w = 4; w < UW; ++w) c[w & 3] = __fmaf_rn(wv[w], xr[jj][v][w], c[w & 3]);
+                                    const float part = (c[0] + c[1]) + (c[2] + c[3]);
+                                    float &a = acc[r * NVP + v];
+                                    if constexpr (F == QMM_Q4_K)
+                                        a = __fmaf_rn(sc, part, __fmaf_rn(-off, xs[jj][v], a));
+                                    else
+                                        a = __fmaf_rn(sc, part, a);
+                                }
+                            }
+                        }
+                    }
+                }
+                const float red = warp_transpose_sum<V>(acc, lane);
+                if (lane < V) pw[i0 * NVP + lane] = red;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->empty[slot]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 
@@ -502,31 +902,123 @@ static cudaError_t launch_gemv_nv(const gv::Params &p, int num_sms, cudaStream_t
     return launch_pdl(gemv_kernel<F, NV>, dim3(grid), dim3(THREADS), smem, st, dim3(1, 1, 1), p);
 }
 
-template <int F>
-static cudaError_t launch_gemv_f(const gv::Params &p, int n, int num_sms, cudaStream_t st) {
-    switch (n) {
-    case 1: return launch_gemv_nv<F, 1>(p, num_sms, st);
-    case 2: return launch_gemv_nv<F, 2>(p, num_sms, st);
-    case 3: return launch_gemv_nv<F, 3>(p, num_sms, st);
-    case 4: return launch_gemv_nv<F, 4>(p, num_sms, st);
-    case 5: return launch_gemv_nv<F, 5>(p, num_sms, st);
-    case 6: return launch_gemv_nv<F, 6>(p, num_sms, st);
-    case 7: return launch_gemv_nv<F, 7>(p, num_sms, st);
-    case 8: return launch_gemv_nv<F, 8>(p, num_sms, st);
+// Register-X plan: k team size TK, units per thread J, rows per team and
+// stage RT; false when X does not fit in registers (then the shared-memory X
+// kernel runs).
+template <int F, int NV> static bool plan_rx(gr::Params &p, int num_sms) {
+    using namespace gr;
+    constexpr int UW = Unit<F>::W;
+    constexpr int JM = jmax<F, NV>();
+    if (NV * UW > XREG) return false;
+    // short rows: the shared-memory X kernel has the shorter start-up and wins
+    if (p.k < 2048) return false;
+    if (p.k % UW != 0) return false;
+    const int64_t nunits = p.k / UW;
+    // a team of TK threads covers k exactly with J units each (J <= JM)
+    int best_tk = 0, best_j = 0;
+    for (int tk = NT; tk >= 32; tk /= 2) {
+        if (nunits % tk == 0 && nunits / tk <= JM) {
+            best_tk = tk;
+            best_j = static_cast<int>(nunits / tk);
+            break;
+        }
+    }
+    if (best_tk == 0) return false;
+    p.tk = best_tk;
+    p.J = best_j;
+    p.teams = NT / best_tk;
+    const int rt_max = PART / nv_pow2<NV>();
+    const int64_t rows_total = static_cast<int64_t>(p.rows_per_mat) * p.mats;
+    // rows per team: enough stages for every SM, stages of about 40 KB at most
+    int64_t rt = rows_total / (static_cast<int64_t>(p.teams) * num_sms);
+    rt = std::min<int64_t>(rt, 40960 / (static_cast<int64_t>(p.teams) * std::max<int64_t>(p.rb, 1)));
+    rt = std::max<int64_t>(4, std::min<int64_t>(rt, rt_max)) / 4 * 4;  // whole groups of four rows
+    p.rt = static_cast<int>(rt);
+    p.stage_rows = p.teams * p.rt;
+    p.stages_per_mat = (p.rows_per_mat + p.stage_rows - 1) / p.stage_rows;
+    p.total_stages = p.stages_per_mat * p.mats;
+    p.stage_bytes = static_cast<int>((static_cast<int64_t>(p.stage_rows) * p.rb + 15 + 15) / 16 * 16);
+    const int fixed = static_cast<int>(sizeof(Ctl)) + 1024;
+    const int per_stage = p.stage_bytes + COMPUTE_WARPS * PART * 4;
+    p.ring = std::min(MAX_RING, (SMEM_BUDGET - fixed) / per_stage);
+    return p.ring >= 2;
+}
+
+template <int F, int NV, int J> static cudaError_t launch_rx_j(const gr::Params &p, int num_sms, cudaStream_t st) {
+    using namespace gr;
+    const size_t smem = 128 + static_cast<size_t>(p.ring) * (p.stage_bytes + COMPUTE_WARPS * PART * 4) + sizeof(Ctl) + 16;
+    cudaError_t e = cudaFuncSetAttribute(gemv_rx_kernel<F, NV, J>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const int grid = std::min(p.total_stages, num_sms);
+    return launch_pdl(gemv_rx_kernel<F, NV, J>, dim3(grid), dim3(THREADS), smem, st, dim3(1, 1, 1), p);
+}
+
+template <int F, int NV> static cudaError_t launch_rx(const gr::Params &p, int num_sms, cudaStream_t st) {
+    constexpr int JM = gr::jmax<F, NV>();
+    switch (p.J) {
+    case 1: return launch_rx_j<F, NV, 1>(p, num_sms, st);
+    case 2: if constexpr (JM >= 2) return launch_rx_j<F, NV, 2>(p, num_sms, st); else return cudaErrorInvalidValue;
+    case 3: if constexpr (JM >= 3) return launch_rx_j<F, NV, 3>(p, num_sms, st); else return cudaErrorInvalidValue;
+    case 4: if constexpr (JM >= 4) return launch_rx_j<F, NV, 4>(p, num_sms, st); else return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
     }
 }
 
-static cudaError_t dispatch(int dtype, const gv::Params &p, int n, int num_sms, cudaStream_t st) {
-    switch (dtype) {
-    case QMM_F32: return launch_gemv_f<QMM_F32>(p, n, num_sms, st);
-    case QMM_Q4_0: return launch_gemv_f<QMM_Q4_0>(p, n, num_sms, st);
-    case QMM_Q8_0: return launch_gemv_f<QMM_Q8_0>(p, n, num_sms, st);
-    case QMM_Q4_K: return launch_gemv_f<QMM_Q4_K>(p, n, num_sms, st);
-    case QMM_Q6_K: return launch_gemv_f<QMM_Q6_K>(p, n, num_sms, st);
-    case QMM_NVFP4: return launch_gemv_f<QMM_NVFP4>(p, n, num_sms, st);
+// Register-X kernel when its plan exists, else the shared-memory X kernel.
+template <int F, int NV>
+static cudaError_t launch_any(gr::Params rp, const gv::Params &gp, int num_sms, cudaStream_t st) {
+    if constexpr (NV * gr::Unit<F>::W <= gr::XREG) {
+        if (plan_rx<F, NV>(rp, num_sms)) return launch_rx<F, NV>(rp, num_sms, st);
+    }
+    return launch_gemv_nv<F, NV>(gp, num_sms, st);
+}
+
+template <int F>
+static cudaError_t launch_any_f(const gr::Params &rp, const gv::Params &gp, int n, int num_sms, cudaStream_t st) {
+    switch (n) {
+    case 1: return launch_any<F, 1>(rp, gp, num_sms, st);
+    case 2: return launch_any<F, 2>(rp, gp, num_sms, st);
+    case 3: return launch_any<F, 3>(rp, gp, num_sms, st);
+    case 4: return launch_any<F, 4>(rp, gp, num_sms, st);
+    case 5: return launch_any<F, 5>(rp, gp, num_sms, st);
+    case 6: return launch_any<F, 6>(rp, gp, num_sms, st);
+    case 7: return launch_any<F, 7>(rp, gp, num_sms, st);
+    case 8: return launch_any<F, 8>(rp, gp, num_sms, st);
     default: return cudaErrorInvalidValue;
     }
+}
+
+static cudaError_t dispatch_any(int dtype, const gr::Params &rp, const gv::Params &gp, int n, int num_sms,
+                                cudaStream_t st) {
+    switch (dtype) {
+    case QMM_F32: return launch_any_f<QMM_F32>(rp, gp, n, num_sms, st);
+    case QMM_Q4_0: return launch_any_f<QMM_Q4_0>(rp, gp, n, num_sms, st);
+    case QMM_Q8_0: return launch_any_f<QMM_Q8_0>(rp, gp, n, num_sms, st);
+    case QMM_Q4_K: return launch_any_f<QMM_Q4_K>(rp, gp, n, num_sms, st);
+    case QMM_Q6_K: return launch_any_f<QMM_Q6_K>(rp, gp, n, num_sms, st);
+    case QMM_NVFP4: return launch_any_f<QMM_NVFP4>(rp, gp, n, num_sms, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+static gr::Params rx_params(const gv::Params &g) {
+    gr::Params r = {};
+    r.w = g.w;
+    r.w_ptrs = g.w_ptrs;
+    r.scales = g.scales;
+    r.x = g.x;
+    r.dst = g.dst;
+    r.k = g.k;
+    r.rb = g.rb;
+    r.rows_per_mat = g.rows_per_mat;
+    r.mats = g.mats;
+    r.n_pairs = g.n_pairs;
+    r.n_used = g.n_used;
+    r.tokens = g.tokens;
+    r.status = g.status;
+    r.limit_ns = g.limit_ns;
+    return r;
 }
 
 cudaError_t launch_gemv(int dtype, const void *w, int64_t rb, const float *x, float *dst, int64_t m, int64_t k, int n,
@@ -545,7 +1037,7 @@ cudaError_t launch_gemv(int dtype, const void *w, int64_t rb, const float *x, fl
     p.status = status;
     p.limit_ns = limit_ns;
     plan_stages(p, static_cast<int64_t>(n) * k * 4, n <= 2 ? gv::SMEM_BUDGET / 2 : gv::SMEM_BUDGET);
-    return dispatch(dtype, p, n, num_sms, st);
+    return dispatch_any(dtype, rx_params(p), p, n, num_sms, st);
 }
 
 cudaError_t launch_moe_gemv(int dtype, const void *const *w_ptrs, int64_t rb, const float *scales, const float *x,
@@ -566,7 +1058,7 @@ cudaError_t launch_moe_gemv(int dtype, const void *const *w_ptrs, int64_t rb, co
     p.status = status;
     p.limit_ns = limit_ns;
     plan_stages(p, static_cast<int64_t>(tokens) * in_f * 4, gv::SMEM_BUDGET / 2);
-    return dispatch(dtype, p, 1, num_sms, st);
+    return dispatch_any(dtype, rx_params(p), p, 1, num_sms, st);
 }
 
 }  // namespace qmm

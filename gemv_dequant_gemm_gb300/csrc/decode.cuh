@@ -367,4 +367,113 @@ template <> __device__ __forceinline__ void decode32_s<QMM_NVFP4>(uint32_t a, in
     }
 }
 
+// ---------------------------------------------------------------------------
+// dec128_aligned<F, H>: weights 128H .. 128H+127 of a 256-wide raw segment
+// whose first byte is 16-byte aligned in shared memory (row bytes a multiple
+// of 16), as 64 half2 words in k order.  The segment bytes come in with
+// 16-byte loads -- conflict-free across a warp's 32 rows because the row pitch
+// is an odd multiple of 16 bytes -- and every block sits at a compile-time
+// byte offset, so the extraction is static funnel shifts.  Results are the
+// same bits as decode32_s.
+// ---------------------------------------------------------------------------
+template <int NW> __device__ __forceinline__ uint32_t word_at(const uint32_t (&w)[NW], int b) {
+    const int i = b >> 2, sh = (b & 3) * 8;
+    return sh == 0 ? w[i] : __funnelshift_r(w[i], w[i + 1], sh);
+}
+template <int NCH, int NW> __device__ __forceinline__ void lds_chunks(uint32_t a, uint32_t (&w)[NW]) {
+    static_assert(NW >= 4 * NCH + 1, "one spare word");
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+        const uint4 v = lds_v4(a + 16u * i);
+        w[4 * i] = v.x;
+        w[4 * i + 1] = v.y;
+        w[4 * i + 2] = v.z;
+        w[4 * i + 3] = v.w;
+    }
+    w[4 * NCH] = 0u;
+}
+
+template <int F, int H> struct Dec128 {  // formats without an aligned variant: never called
+    static __device__ __forceinline__ void run(uint32_t, uint32_t (&o)[64]) {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) o[i] = 0u;
+    }
+};
+
+template <int H> struct Dec128<QMM_Q4_0, H> {
+    static __device__ __forceinline__ void run(uint32_t a, uint32_t (&o)[64]) {
+        constexpr int LO = H ? 64 : 0, OFF = 72 * H - LO;  // 4 blocks of 18 bytes from byte 72H
+        uint32_t w[21];
+        lds_chunks<5>(a + LO, w);
+        const __half2 off = __floats2half2_rn(1032.0f, 1032.0f);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int b = OFF + 18 * j;
+            const __half2 d2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(word_at(w, b) & 0xFFFFu)));
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const uint32_t v = word_at(w, b + 2 + 4 * t), vh = v >> 4;
+                const uint32_t l01 = (__byte_perm(v, 0, 0x4140) & 0x000F000Fu) | 0x64006400u;
+                const uint32_t l23 = (__byte_perm(v, 0, 0x4342) & 0x000F000Fu) | 0x64006400u;
+                const uint32_t h01 = (__byte_perm(vh, 0, 0x4140) & 0x000F000Fu) | 0x64006400u;
+                const uint32_t h23 = (__byte_perm(vh, 0, 0x4342) & 0x000F000Fu) | 0x64006400u;
+                o[16 * j + 2 * t] = h2_bits(__hmul2(__hsub2(bits_h2(l01), off), d2));
+                o[16 * j + 2 * t + 1] = h2_bits(__hmul2(__hsub2(bits_h2(l23), off), d2));
+                o[16 * j + 8 + 2 * t] = h2_bits(__hmul2(__hsub2(bits_h2(h01), off), d2));
+                o[16 * j + 8 + 2 * t + 1] = h2_bits(__hmul2(__hsub2(bits_h2(h23), off), d2));
+            }
+        }
+    }
+};
+
+template <int H> struct Dec128<QMM_Q8_0, H> {
+    static __device__ __forceinline__ void run(uint32_t a, uint32_t (&o)[64]) {
+        constexpr int LO = H ? 128 : 0, OFF = 136 * H - LO;  // 4 blocks of 34 bytes from byte 136H
+        uint32_t w[37];
+        lds_chunks<9>(a + LO, w);
+        const __half2 off = __floats2half2_rn(1152.0f, 1152.0f);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int b = OFF + 34 * j;
+            const __half2 d2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(word_at(w, b) & 0xFFFFu)));
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const uint32_t v = word_at(w, b + 2 + 4 * t) ^ 0x80808080u;
+                o[16 * j + 2 * t] = h2_bits(__hmul2(__hsub2(bits_h2(__byte_perm(v, 0x64646464u, 0x4140)), off), d2));
+                o[16 * j + 2 * t + 1] =
+                    h2_bits(__hmul2(__hsub2(bits_h2(__byte_perm(v, 0x64646464u, 0x4342)), off), d2));
+            }
+        }
+    }
+};
+
+template <int H> struct Dec128<QMM_NVFP4, H> {
+    static __device__ __forceinline__ void run(uint32_t a, uint32_t (&o)[64]) {
+        constexpr int LO = H ? 64 : 0, OFF = 72 * H - LO;  // 2 groups of 36 bytes from byte 72H
+        uint32_t w[21];
+        lds_chunks<5>(a + LO, w);
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+            const int b = OFF + 36 * g;
+            const uint32_t sc4 = word_at(w, b);
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const __half2 s0 = __float2half2_rn(e4m3_to_f32((sc4 >> (16 * hf)) & 0xFFu));
+                const __half2 s1 = __float2half2_rn(e4m3_to_f32((sc4 >> (16 * hf + 8)) & 0xFFu));
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const uint32_t c = word_at(w, b + 4 + 16 * hf + 4 * t);
+                    const __half2 sv = (t < 2) ? s0 : s1;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t byte = (c >> (8 * i)) & 0xFFu;
+                        const __half2 v = __floats2half2_rn(e2m1_to_f32(byte & 15u), e2m1_to_f32(byte >> 4));
+                        o[32 * g + 16 * hf + 4 * t + i] = h2_bits(__hmul2(v, sv));
+                    }
+                }
+            }
+        }
+    }
+};
+
 }  // namespace qmm

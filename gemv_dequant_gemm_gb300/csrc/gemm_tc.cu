@@ -50,6 +50,8 @@
 #include <cudaTypedefs.h>
 #include <string.h>
 
+#include <algorithm>
+
 #include "decode.cuh"
 #include "kernels.h"
 
@@ -76,17 +78,21 @@ struct Ctl {
     int abort;
 };
 
-// Geometry of a (format, BN) instance: ring depths that fit in shared memory.
-template <int F, int BN> struct Plan {
+// Geometry of a (format, BN, SUB) instance: ring depths that fit in shared
+// memory.  A CTA owns SUB 128-row subtiles (SUB = 2: two accumulators share
+// every X stage, halving the X bytes per MMA).
+template <int F, int BN, int SUB> struct Plan {
     static constexpr bool TF32 = (F == QMM_F32);
+    static_assert(SUB == 1 || (SUB == 2 && !TF32), "two subtiles for packed W only");
+    static constexpr int ROWS = BM * SUB;                  // W rows per CTA
     static constexpr int QK = Fmt<F>::QK, BB = Fmt<F>::BB;
-    // k per MMA stage: packed W takes a whole 256-wide raw unit (16 MMAs of
-    // K=16); f32 W takes 64 (8 MMAs of K=8)
-    static constexpr int KPS = TF32 ? 64 : RK;
+    // k per MMA stage: packed W takes 256/SUB (16 MMAs of K=16 per stage
+    // across the subtiles); f32 W takes 64 (8 MMAs of K=8)
+    static constexpr int KPS = TF32 ? 64 : RK / SUB;
     static constexpr int ELEM = TF32 ? 4 : 2;
     static constexpr int ATOMS = KPS * ELEM / ATOM_ROW;   // swizzle atoms along k per stage
     static constexpr int KMMA = TF32 ? 8 : 16;
-    static constexpr int MMAS = KPS / KMMA;               // MMAs per stage
+    static constexpr int MMAS = KPS / KMMA;               // MMAs per stage and subtile
     static constexpr int B_ATOM = BN * ATOM_ROW;
     static constexpr int B_STAGE = ATOMS * B_ATOM;
     static constexpr int A_ATOM = BM * ATOM_ROW;
@@ -97,27 +103,29 @@ template <int F, int BN> struct Plan {
     static constexpr int SLACK = (F == QMM_Q4_K) ? 0 : ((F == QMM_NVFP4) ? 12 : 14);
     static constexpr int P0 = TF32 ? 16 : (RB + SLACK + 15) / 16 * 16;
     static constexpr int P = ((P0 / 16) % 2 == 1) ? P0 : P0 + 16;
-    static constexpr int RAW_STAGE = TF32 ? 0 : BM * P;
+    static constexpr int RAW_STAGE = TF32 ? 0 : ROWS * P;
     static constexpr int CTL = static_cast<int>(sizeof(Ctl));
-    // raw stages: three when that still leaves room for two X stages, else two
-    static constexpr int RS = TF32 ? 0 : ((SMEM_LIMIT - 1024 - CTL - 3 * RAW_STAGE >= 2 * B_STAGE) ? 3 : 2);
+    // raw stages: three when that still leaves 128 KB for X stages, else two
+    static constexpr int RS = TF32 ? 0 : ((SMEM_LIMIT - 1024 - CTL - 3 * RAW_STAGE >= 131072) ? 3 : 2);
     static constexpr int AVAIL = SMEM_LIMIT - 1024 - CTL - RS * RAW_STAGE;
     // X (and f32 W) stages: as many as fit, at most MAXS
     static constexpr int BS0 = AVAIL / (B_STAGE + A_STAGE);
     static constexpr int BS = BS0 > MAXS ? MAXS : BS0;
-    // decoded-W (A) stages: packed W in tensor memory after the accumulator
-    // (KPS/2 columns each: two f16 per column); f32 W with the X stages
-    static constexpr int A_COLS = KPS / 2;
-    static constexpr int AS0 = TF32 ? BS : (TMEM_MAX - BN) / A_COLS;
+    // decoded-W (A) stages: packed W in tensor memory after the SUB
+    // accumulators (SUB * KPS/2 columns each: two f16 per column, subtile t at
+    // +64t); f32 W with the X stages
+    static constexpr int D_COLS = SUB * BN;
+    static constexpr int A_COLS = SUB * KPS / 2;
+    static constexpr int AS0 = TF32 ? BS : (TMEM_MAX - D_COLS) / A_COLS;
     static constexpr int AS = AS0 > MAXS ? MAXS : AS0;
     static constexpr int RING = BS * (B_STAGE + A_STAGE) + RS * RAW_STAGE;
     static constexpr int TMEM_COLS = TF32 ? BN : TMEM_MAX;
-    static constexpr int RED = BM * BN * 4;               // split-K partial tile (aliases the rings)
+    static constexpr int RED = ROWS * BN * 4;             // split-K partial tile (aliases the rings)
     static constexpr int BODY = RING > RED ? RING : RED;
     static constexpr size_t SMEM = 1024 + BODY + sizeof(Ctl);
     static_assert(TF32 || RS >= 2, "raw ring needs two stages");
     static_assert(BS >= 2 && AS >= 2, "rings need two stages");
-    static_assert(TF32 || BN + AS * A_COLS <= TMEM_MAX, "A slots exceed tensor memory");
+    static_assert(TF32 || D_COLS + AS * A_COLS <= TMEM_MAX, "A slots exceed tensor memory");
     static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0 && TMEM_COLS >= 32 && TMEM_COLS <= 512, "TMEM allocation");
     static_assert(SMEM <= SMEM_LIMIT, "shared memory plan too large");
     static constexpr uint32_t IDESC = mma_idesc(TF32 ? 2u : 0u, BM, BN);
@@ -148,12 +156,13 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
     return r;
 }
+// (no memory clobber: the partials were published by the cluster barrier
+// before the first of these loads and are not written again until the next one)
 __device__ __forceinline__ float4 ld_dsmem_v4(uint32_t addr) {
     float4 v;
     asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
                  : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr)
-                 : "memory");
+                 : "r"(addr));
     return v;
 }
 __device__ __forceinline__ int ld_dsmem_u32(uint32_t addr) {
@@ -171,19 +180,22 @@ struct GemmParams {
     int w_early; // 1: the kernel before this one only wrote the f16 copy of X, so W may be read before it ends
     int raw_g;   // rows per 16-byte-aligned row group of the raw-weight tensor map; 0 = per-row bulk copies
     int splits;  // CTAs per output tile (cluster size along z)
+    int x3d;     // 1: X (and f32 W) maps are 3-D [k atoms][rows][atom]: one TMA request per stage
+    int dtma;    // 1: the tile is stored with one TMA store through tmap_d (m % 4 == 0)
     uint32_t *status;
     uint64_t limit_ns;
     int debug_skip;
 };
 
-template <int F, int BN>
+template <int F, int BN, int SUB>
 __global__ void __launch_bounds__(gemm::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
-                   const __grid_constant__ CUtensorMap tmap_raw, const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmap_raw, const __grid_constant__ CUtensorMap tmap_d,
+                   const GemmParams p) {
     using namespace gemm;
-    using PL = Plan<F, BN>;
+    using PL = Plan<F, BN, SUB>;
     constexpr bool TF32 = PL::TF32;
-    constexpr int KPS = PL::KPS, BS = PL::BS, AS = PL::AS, RS = PL::RS;
+    constexpr int KPS = PL::KPS, BS = PL::BS, AS = PL::AS, RS = PL::RS, ROWS = PL::ROWS;
     constexpr int SPU = RK / KPS;  // MMA stages per 256-wide unit
 
     extern __shared__ uint8_t smem_raw[];
@@ -195,7 +207,7 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
     Ctl *ctl = reinterpret_cast<Ctl *>(base + PL::BODY);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
+    const int m0 = blockIdx.x * ROWS, n0 = blockIdx.y * BN;
     const int S = p.splits;
     const int z = (S > 1) ? static_cast<int>(cluster_rank()) : 0;
     const int u0 = z * p.units / S, u1 = (z + 1) * p.units / S;
@@ -249,14 +261,14 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
                 uint8_t *stage = sRaw + r * PL::RAW_STAGE;
                 if (p.raw_g > 0) {
                     // one 2-D TMA box per row residue g: rows m0+g, m0+g+G, ... land
-                    // contiguously at slots g*(BM/G) ... with pitch P
+                    // contiguously at slots g*(ROWS/G) ... with pitch P
                     if (lane == 0) {
                         const int G = p.raw_g;
-                        mbar_arrive_expect_tx(&ctl->raw_full[r], BM * PL::P);
+                        mbar_arrive_expect_tx(&ctl->raw_full[r], ROWS * PL::P);
                         for (int g = 0; g < G; ++g) {
                             const int64_t xb = (static_cast<int64_t>(g) * p.rb + seg_off) & ~int64_t(15);
-                            tma_load_2d(stage + g * (BM / G) * PL::P, &tmap_raw, static_cast<int32_t>(xb / 2), m0 / G,
-                                        &ctl->raw_full[r]);
+                            tma_load_2d(stage + g * (ROWS / G) * PL::P, &tmap_raw, static_cast<int32_t>(xb / 2),
+                                        m0 / G, &ctl->raw_full[r]);
                         }
                     }
                     __syncwarp();
@@ -264,11 +276,11 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
                     continue;
                 }
                 const int len = static_cast<int>(min(static_cast<int64_t>(PL::RB), p.rb - seg_off));
-                uint32_t bytes[4];
-                const uint8_t *src[4];
+                uint32_t bytes[ROWS / 32];
+                const uint8_t *src[ROWS / 32];
                 uint32_t tot = 0;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int j = 0; j < ROWS / 32; ++j) {
                     const int row = lane + 32 * j, gm = m0 + row;
                     bytes[j] = 0;
                     src[j] = nullptr;
@@ -286,7 +298,7 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
                 if (lane == 0) mbar_arrive_expect_tx(&ctl->raw_full[r], tot);
                 __syncwarp();
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
+                for (int j = 0; j < ROWS / 32; ++j)
                     if (bytes[j]) bulk_load_1d(stage + (lane + 32 * j) * PL::P, src[j], bytes[j], &ctl->raw_full[r]);
                 last[r] = i;
             }
@@ -308,11 +320,19 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
                 if (!mbar_wait_bounded(&ctl->b_empty[s], ph ^ 1, abort, p.status, p.limit_ns)) break;
                 if (p.debug_skip && i == 0) continue;  // test hook: stage 0 never fills
                 mbar_arrive_expect_tx(&ctl->b_full[s], PL::B_STAGE + PL::A_STAGE);
+                if (p.x3d) {
+                    // the whole stage (every 128-byte k atom of the tile rows) in one request:
+                    // one SM's TMA engine spends about the same time per request up to 32 KB
+                    if constexpr (TF32) tma_load_3d(sA + s * PL::A_STAGE, &tmap_w, 0, m0, kt * PL::ATOMS, &ctl->b_full[s]);
+                    tma_load_3d(sB + s * PL::B_STAGE, &tmap_x, 0, n0, kt * PL::ATOMS, &ctl->b_full[s]);
+                } else {
 #pragma unroll
-                for (int j = 0; j < PL::ATOMS; ++j) {
-                    const int kx = kt * KPS + j * (ATOM_ROW / PL::ELEM);
-                    if constexpr (TF32) tma_load_2d(sA + s * PL::A_STAGE + j * PL::A_ATOM, &tmap_w, kx, m0, &ctl->b_full[s]);
-                    tma_load_2d(sB + s * PL::B_STAGE + j * PL::B_ATOM, &tmap_x, kx, n0, &ctl->b_full[s]);
+                    for (int j = 0; j < PL::ATOMS; ++j) {
+                        const int kx = kt * KPS + j * (ATOM_ROW / PL::ELEM);
+                        if constexpr (TF32)
+                            tma_load_2d(sA + s * PL::A_STAGE + j * PL::A_ATOM, &tmap_w, kx, m0, &ctl->b_full[s]);
+                        tma_load_2d(sB + s * PL::B_STAGE + j * PL::B_ATOM, &tmap_x, kx, n0, &ctl->b_full[s]);
+                    }
                 }
                 last[s] = i;
             }
@@ -332,18 +352,22 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
                 tc_fence_after();
                 const uint32_t b_addr = smem_u32(sB + sb * PL::B_STAGE);
 #pragma unroll
-                for (int kk = 0; kk < PL::MMAS; ++kk) {
-                    // K step kk: atom kk/4, 32 bytes (16 f16 or 8 f32) per step inside the atom
-                    const uint32_t off = static_cast<uint32_t>((kk >> 2) * PL::B_ATOM + 32 * (kk & 3));
-                    const uint64_t bd = sw128_desc(b_addr + off);
-                    if constexpr (TF32) {
-                        const uint32_t aoff = static_cast<uint32_t>((kk >> 2) * PL::A_ATOM + 32 * (kk & 3));
-                        const uint64_t ad = sw128_desc(smem_u32(sA + sa * PL::A_STAGE) + aoff);
-                        mma_tf32(tmem, ad, bd, PL::IDESC, (i | kk) != 0);
-                    } else {
-                        // A slot sa: A_COLS columns after the accumulator, 8 per K=16 step
-                        const uint32_t at = tmem + BN + static_cast<uint32_t>(sa * PL::A_COLS + 8 * kk);
-                        mma_f16_tmem_a(tmem, at, bd, PL::IDESC, (i | kk) != 0);
+                for (int t = 0; t < SUB; ++t) {  // subtiles share every X stage
+#pragma unroll
+                    for (int kk = 0; kk < PL::MMAS; ++kk) {
+                        // K step kk: atom kk/4, 32 bytes (16 f16 or 8 f32) per step inside the atom
+                        const uint32_t off = static_cast<uint32_t>((kk >> 2) * PL::B_ATOM + 32 * (kk & 3));
+                        const uint64_t bd = sw128_desc(b_addr + off);
+                        if constexpr (TF32) {
+                            const uint32_t aoff = static_cast<uint32_t>((kk >> 2) * PL::A_ATOM + 32 * (kk & 3));
+                            const uint64_t ad = sw128_desc(smem_u32(sA + sa * PL::A_STAGE) + aoff);
+                            mma_tf32(tmem, ad, bd, PL::IDESC, (i | kk) != 0);
+                        } else {
+                            // A slot sa after the accumulators: subtile t at +64t, 8 columns per K=16 step
+                            const uint32_t at =
+                                tmem + PL::D_COLS + static_cast<uint32_t>(sa * PL::A_COLS + 64 * t + 8 * kk);
+                            mma_f16_tmem_a(tmem + static_cast<uint32_t>(t * BN), at, bd, PL::IDESC, (i | kk) != 0);
+                        }
                     }
                 }
                 mma_commit(&ctl->b_empty[sb]);
@@ -354,49 +378,66 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
         __syncwarp();
     } else {
         // ------------- decode warps -------------
-        // Thread = W row 32*(warp%4) + lane = TMEM lane; warps 3-6 decode the
-        // first 128 k of every 256-wide stage, warps 7-10 the second.
+        // Thread = one W row = one TMEM lane (lane quarter warp%4).  SUB == 1:
+        // warps 3-6 decode the first 128 k of every 256-wide stage, warps 7-10
+        // the second.  SUB == 2: warps 3-6 decode subtile 0 (rows 0-127),
+        // warps 7-10 subtile 1, each the whole 128-wide stage.
         if constexpr (!TF32) {
-            static_assert(KPS == RK, "one raw unit per MMA stage");
+            constexpr int SPU_ = RK / KPS;  // MMA stages per raw unit (= SUB)
             const int q = warp & 3;
             const int hh = (warp - WARP_DEC0) >> 2;
-            const int row = 32 * q + lane;
-            const int slot = (p.raw_g > 0) ? (row % p.raw_g) * (BM / p.raw_g) + row / p.raw_g : row;
+            const int row = (SUB == 2 ? 128 * hh : 0) + 32 * q + lane;
+            const int slot = (p.raw_g > 0) ? (row % p.raw_g) * (ROWS / p.raw_g) + row / p.raw_g : row;
             const uint32_t rowoff = static_cast<uint32_t>(slot * PL::P);
             const int gm = m0 + row;
             const uint32_t misb = static_cast<uint32_t>(
                 (reinterpret_cast<uintptr_t>(p.w) + static_cast<int64_t>(gm < p.M ? gm : 0) * p.rb) & 15u);
             const uint32_t raw0 = smem_u32(sRaw);
-            const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16) + BN + 64u * hh;
+            const uint32_t tq = tmem + (static_cast<uint32_t>(32 * q) << 16) + PL::D_COLS + 64u * hh;
             for (int i = 0; i < NK; ++i) {
-                const int kt = kt0 + i, sa = i % AS, r = i % RS;
-                {
-                    const bool ok = mbar_wait_bounded(&ctl->raw_full[r], (i / RS) & 1, abort, p.status, p.limit_ns);
+                const int kt = kt0 + i, sa = i % AS;
+                const int unit = kt / SPU_, ui = unit - u0, r = ui % RS;
+                if (kt % SPU_ == 0) {
+                    const bool ok = mbar_wait_bounded(&ctl->raw_full[r], (ui / RS) & 1, abort, p.status, p.limit_ns);
                     if (!__all_sync(0xFFFFFFFFu, ok)) break;
                 }
                 const bool ok = mbar_wait_bounded(&ctl->a_empty[sa], ((i / AS) & 1) ^ 1, abort, p.status, p.limit_ns);
                 if (!__all_sync(0xFFFFFFFFu, ok)) break;
                 tc_fence_after();
-                const uint32_t mis = (misb + static_cast<uint32_t>(kt * PL::RB)) & 15u;
+                const uint32_t mis = (misb + static_cast<uint32_t>(unit * PL::RB)) & 15u;
                 const uint32_t src = raw0 + static_cast<uint32_t>(r * PL::RAW_STAGE) + rowoff + mis;
+                const int H = (SUB == 2) ? (kt % SPU_) : hh;  // which 128-wide half of the unit
+                uint32_t o[64];
+                constexpr bool kAligned = (F == QMM_Q4_0 || F == QMM_Q8_0 || F == QMM_NVFP4);
+                if (kAligned && mis == 0 && gm < p.M && static_cast<int64_t>(unit) * RK + 128 * H + 128 <= p.K) {
+                    // 16-byte aligned segment: conflict-free 16-byte loads, static offsets
+                    if (H == 0)
+                        Dec128<F, 0>::run(src, o);
+                    else
+                        Dec128<F, 1>::run(src, o);
+                } else {
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const int e0 = 128 * hh + 32 * t;  // within the 256-wide unit
-                    uint32_t o[16];
-                    if (gm < p.M && static_cast<int64_t>(kt) * RK + e0 < p.K) {
-                        decode32_s<F>(src, e0, o);
-                    } else {
+                    for (int t = 0; t < 4; ++t) {
+                        const int e0 = 128 * H + 32 * t;  // weights within the 256-wide unit
+                        uint32_t ot[16];
+                        if (gm < p.M && static_cast<int64_t>(unit) * RK + e0 < p.K) {
+                            decode32_s<F>(src, e0, ot);
+                        } else {
 #pragma unroll
-                        for (int q2 = 0; q2 < 16; ++q2) o[q2] = 0u;
+                            for (int q2 = 0; q2 < 16; ++q2) ot[q2] = 0u;
+                        }
+#pragma unroll
+                        for (int q2 = 0; q2 < 16; ++q2) o[16 * t + q2] = ot[q2];
                     }
-                    tmem_st_32x32b_x16(tq + static_cast<uint32_t>(sa * PL::A_COLS + 16 * t), o);
                 }
+                tmem_st_32x32b_x64(tq + static_cast<uint32_t>(sa * PL::A_COLS), o);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&ctl->a_full[sa]);
-                    mbar_arrive(&ctl->raw_empty[r]);
+                    // the last stage of a raw unit (or of this CTA) frees the raw stage
+                    if (kt % SPU_ == SPU_ - 1 || i == NK - 1) mbar_arrive(&ctl->raw_empty[r]);
                 }
             }
         }
@@ -410,17 +451,45 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
         if (!drained) *abort = 1;
         have = __all_sync(0xFFFFFFFFu, drained && !*abort);  // tcgen05.ld is warp-collective
     }
+    // Warp (quarter q, half hh) stores: SUB == 1: rows 32q+lane, columns
+    // [BN/2*hh, BN/2*hh + BN/2); SUB == 2: rows 128hh + 32q + lane (subtile hh,
+    // accumulator at TMEM column BN*hh), all BN columns.
     const int q = warp & 3;                                           // TMEM lane quarter of this warp
-    const int colbase = (warp >= WARP_DEC0 + 4) ? BN / 2 : 0;
-    const int rloc = 32 * q + lane;                                   // tile row of this thread
-    if (S == 1) {
+    const int hh = (warp >= WARP_DEC0 + 4) ? 1 : 0;
+    constexpr int ECOLS = (SUB == 2) ? BN : BN / 2;                   // output columns per warp
+    const int colbase = (SUB == 2) ? 0 : (BN / 2) * hh;               // first output column in the tile
+    const uint32_t dcol = static_cast<uint32_t>((SUB == 2) ? BN * hh : (BN / 2) * hh);  // its TMEM column
+    const int rloc = (SUB == 2 ? 128 * hh : 0) + 32 * q + lane;      // tile row of this thread
+    if (S == 1 && p.dtma) {
+        // tile -> shared memory as [BN][ROWS] (m contiguous), then one TMA store
+        if (is_epi) {
+            if (have) {
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < ECOLS / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + dcol + 32 * c, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) sRed[(colbase + 32 * c + j) * ROWS + rloc] = __uint_as_float(v[j]);
+                }
+            }
+            fence_proxy_async_smem();  // the generic-proxy writes above, before the async-proxy read
+            asm volatile("bar.sync 1, %0;" ::"r"(32 * NUM_DECODE_WARPS) : "memory");  // every epilogue warp
+            if (warp == WARP_DEC0 && lane == 0 && !*abort) {
+                tma_store_2d(&tmap_d, m0, n0, sRed);
+                bulk_commit_group();
+                bulk_wait_group_read0();  // the source stays valid until the engine has read it
+            }
+        }
+    } else if (S == 1) {
         if (is_epi && have) {
             tc_fence_after();
             const int gm = m0 + rloc;
 #pragma unroll 1
-            for (int c = 0; c < BN / 2 / 32; ++c) {
+            for (int c = 0; c < ECOLS / 32; ++c) {
                 uint32_t v[32];
-                tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + colbase + 32 * c, v);
+                tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + dcol + 32 * c, v);
                 tmem_ld_wait();
                 const int gn0 = n0 + colbase + 32 * c;
                 if (gm < p.M) {
@@ -431,16 +500,16 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
             }
         }
     } else {
-        // partial tile -> own shared memory, column-major [BN][BM]
+        // partial tile -> own shared memory, column-major [BN][ROWS]
         if (is_epi && have) {
             tc_fence_after();
 #pragma unroll 1
-            for (int c = 0; c < BN / 2 / 32; ++c) {
+            for (int c = 0; c < ECOLS / 32; ++c) {
                 uint32_t v[32];
-                tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + colbase + 32 * c, v);
+                tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + dcol + 32 * c, v);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) sRed[(colbase + 32 * c + j) * BM + rloc] = __uint_as_float(v[j]);
+                for (int j = 0; j < 32; ++j) sRed[(colbase + 32 * c + j) * ROWS + rloc] = __uint_as_float(v[j]);
             }
         }
         __syncwarp();
@@ -453,16 +522,23 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
         const int c0 = z * cols;
         const uint32_t red0 = smem_u32(sRed);
         const bool vec = (p.M % 4) == 0;
-        for (int it = any_abort ? THREADS * BN : threadIdx.x; it < cols * (BM / 4); it += THREADS) {
-            const int cl = c0 + it / (BM / 4), r4 = (it % (BM / 4)) * 4;
-            const uint32_t off = static_cast<uint32_t>((cl * BM + r4) * 4);
-            float4 acc = ld_dsmem_v4(mapa_shared(red0 + off, 0));
-            for (int pr = 1; pr < S; ++pr) {
-                const float4 v = ld_dsmem_v4(mapa_shared(red0 + off, static_cast<uint32_t>(pr)));
-                acc.x += v.x;
-                acc.y += v.y;
-                acc.z += v.z;
-                acc.w += v.w;
+        for (int it = any_abort ? cols * (ROWS / 4) : threadIdx.x; it < cols * (ROWS / 4); it += THREADS) {
+            const int cl = c0 + it / (ROWS / 4), r4 = (it % (ROWS / 4)) * 4;
+            const uint32_t off = static_cast<uint32_t>((cl * ROWS + r4) * 4);
+            // all peers' loads in flight first, then the sum in rank order
+            float4 v[MAX_SPLIT];
+#pragma unroll
+            for (int pr = 0; pr < MAX_SPLIT; ++pr)
+                if (pr < S) v[pr] = ld_dsmem_v4(mapa_shared(red0 + off, static_cast<uint32_t>(pr)));
+            float4 acc = v[0];
+#pragma unroll
+            for (int pr = 1; pr < MAX_SPLIT; ++pr) {
+                if (pr < S) {
+                    acc.x += v[pr].x;
+                    acc.y += v[pr].y;
+                    acc.z += v[pr].z;
+                    acc.w += v[pr].w;
+                }
             }
             const int gn = n0 + cl, gm = m0 + r4;
             if (gn < p.N && gm < p.M) {
@@ -533,11 +609,32 @@ static bool make_map(CUtensorMap *map, const void *ptr, CUtensorMapDataType dt, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D view of a row-major [rows][cols] matrix as [cols/A][rows][A] with A the
+// elements of one 128-byte swizzle atom (the atom index outermost, stride 128
+// bytes): a box [A][box_rows][atoms] lands as `atoms` consecutive
+// [box_rows x 128 B] swizzled atoms, i.e. one request per pipeline stage.
+// Needs cols % A == 0 (else the last atom of a row would alias the next row).
+static bool make_map_3d(CUtensorMap *map, const void *ptr, CUtensorMapDataType dt, int elem, int64_t rows,
+                        int64_t cols, int box_rows, int atoms) {
+    auto fn = get_encode_fn();
+    const int A = 128 / elem;
+    if (!fn || cols % A != 0) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(A), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(cols / A)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * elem, 128};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(A), static_cast<cuuint32_t>(box_rows),
+                               static_cast<cuuint32_t>(atoms)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, dt, 3, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Raw packed-weight map: the [m][rb] bytes viewed as [m/G][G*rb/2] uint16 with
 // G the smallest row group whose byte stride is a multiple of 16; boxes of
-// [BM/G][P/2] (P bytes per row, no swizzle).  Returns G, or 0 when no such
-// view exists (then the kernel copies row by row).
-static int make_raw_map(CUtensorMap *map, const void *w, int64_t m, int64_t rb, int pitch) {
+// [rows/G][P/2] (P bytes per row, no swizzle; `rows` W rows per CTA).  Returns
+// G, or 0 when no such view exists (then the kernel copies row by row).
+static int make_raw_map(CUtensorMap *map, const void *w, int64_t m, int64_t rb, int pitch, int rows) {
     auto fn = get_encode_fn();
     if (!fn) return 0;
     int G = 1;
@@ -545,7 +642,7 @@ static int make_raw_map(CUtensorMap *map, const void *w, int64_t m, int64_t rb, 
     if (G > 8 || m % G != 0 || pitch % 16 != 0 || pitch / 2 > 256) return 0;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(G * rb / 2), static_cast<cuuint64_t>(m / G)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(G * rb)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(pitch / 2), static_cast<cuuint32_t>(gemm::BM / G)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(pitch / 2), static_cast<cuuint32_t>(rows / G)};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(w), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -553,9 +650,9 @@ static int make_raw_map(CUtensorMap *map, const void *w, int64_t m, int64_t rb, 
     return r == CUDA_SUCCESS ? G : 0;
 }
 
-template <int F, int BN> static cudaError_t set_attr() {
-    return cudaFuncSetAttribute(gemm_tc_kernel<F, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(gemm::Plan<F, BN>::SMEM));
+template <int F, int BN, int SUB> static cudaError_t set_attr() {
+    return cudaFuncSetAttribute(gemm_tc_kernel<F, BN, SUB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(gemm::Plan<F, BN, SUB>::SMEM));
 }
 
 // Opt every instance into its shared-memory carve-out; called once per device
@@ -565,12 +662,17 @@ cudaError_t gemm_tc_init() {
     auto chk = [&](cudaError_t r) {
         if (e == cudaSuccess) e = r;
     };
-    chk(set_attr<QMM_F32, 128>());
-    chk(set_attr<QMM_Q4_0, 128>());
-    chk(set_attr<QMM_Q8_0, 128>());
-    chk(set_attr<QMM_Q4_K, 128>());
-    chk(set_attr<QMM_Q6_K, 128>());
-    chk(set_attr<QMM_NVFP4, 128>());
+    chk(set_attr<QMM_F32, 128, 1>());
+    chk(set_attr<QMM_Q4_0, 128, 1>());
+    chk(set_attr<QMM_Q8_0, 128, 1>());
+    chk(set_attr<QMM_Q4_K, 128, 1>());
+    chk(set_attr<QMM_Q6_K, 128, 1>());
+    chk(set_attr<QMM_NVFP4, 128, 1>());
+    chk(set_attr<QMM_Q4_0, 128, 2>());
+    chk(set_attr<QMM_Q8_0, 128, 2>());
+    chk(set_attr<QMM_Q4_K, 128, 2>());
+    chk(set_attr<QMM_Q6_K, 128, 2>());
+    chk(set_attr<QMM_NVFP4, 128, 2>());
     return e;
 }
 
@@ -582,29 +684,59 @@ static int choose_splits(int64_t tiles, int units, int num_sms) {
     return s;
 }
 
+template <int F, int SUB>
+static cudaError_t launch_sub(const GemmArgs &a, GemmParams p, int num_sms, cudaStream_t st) {
+    using namespace gemm;
+    constexpr int BN = 128;
+    using PL = Plan<F, BN, SUB>;
+    CUtensorMap map_x, map_w, map_raw;
+    memset(&map_w, 0, sizeof(map_w));
+    memset(&map_raw, 0, sizeof(map_raw));
+    const void *xsrc = (F == QMM_F32) ? static_cast<const void *>(a.x) : a.x16;
+    const CUtensorMapDataType xdt = (F == QMM_F32) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    p.x3d = make_map_3d(&map_x, xsrc, xdt, PL::ELEM, a.n, a.k, BN, PL::ATOMS) &&
+            (F != QMM_F32 || make_map_3d(&map_w, a.w, xdt, PL::ELEM, a.m, a.k, BM, PL::ATOMS));
+    if (!p.x3d) {
+        if (!make_map(&map_x, xsrc, xdt, PL::ELEM, a.n, a.k, BN, ATOM_ROW / PL::ELEM)) return cudaErrorInvalidValue;
+        if (F == QMM_F32 && !make_map(&map_w, a.w, xdt, PL::ELEM, a.m, a.k, BM, ATOM_ROW / PL::ELEM))
+            return cudaErrorInvalidValue;
+    }
+    if (F != QMM_F32) map_w = map_x;  // unused by the packed-format kernels
+    p.raw_g = (F == QMM_F32) ? 0 : make_raw_map(&map_raw, a.w, a.m, a.rb, PL::P, PL::ROWS);
+    const int64_t m_tiles = (a.m + PL::ROWS - 1) / PL::ROWS, n_tiles = (a.n + BN - 1) / BN;
+    p.splits = choose_splits(m_tiles * n_tiles, p.units, num_sms);
+    // dst [n][m] f32 viewed by a TMA store map: boxes of [BN n][ROWS m]
+    CUtensorMap map_d;
+    memset(&map_d, 0, sizeof(map_d));
+    p.dtma = 0;
+    if (a.m % 4 == 0) {
+        auto fn = get_encode_fn();
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.m), static_cast<cuuint64_t>(a.n)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.m) * 4};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(PL::ROWS), static_cast<cuuint32_t>(BN)};
+        const cuuint32_t estr[2] = {1, 1};
+        p.dtma = fn && fn(&map_d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.dst, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
+    const dim3 grid(static_cast<unsigned>(m_tiles), static_cast<unsigned>(n_tiles), static_cast<unsigned>(p.splits));
+    const dim3 cluster(1, 1, static_cast<unsigned>(p.splits));
+    return launch_pdl(gemm_tc_kernel<F, BN, SUB>, grid, dim3(THREADS), PL::SMEM, st, cluster, map_x, map_w, map_raw,
+                      map_d, p);
+}
+
 template <int F>
 static cudaError_t launch_gemm_t(const GemmArgs &a, int num_sms, cudaStream_t st) {
     using namespace gemm;
     constexpr int BN = 128;
-    using PL = Plan<F, BN>;
-    CUtensorMap map_x, map_w, map_raw;
-    memset(&map_w, 0, sizeof(map_w));
-    memset(&map_raw, 0, sizeof(map_raw));
     bool pdl = false;
-    int raw_g = 0;
-    if (F == QMM_F32) {
-        if (!make_map(&map_x, a.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.n, a.k, BN, 32)) return cudaErrorInvalidValue;
-        if (!make_map(&map_w, a.w, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.m, a.k, BM, 32)) return cudaErrorInvalidValue;
-    } else {
+    if (F != QMM_F32) {
         const int64_t total8 = a.n * a.k / 8;
         const int64_t want = (total8 + 255) / 256;
         const int grid = static_cast<int>(want < 8LL * num_sms ? want : 8LL * num_sms);
         cudaError_t e = launch_pdl(x_to_f16_kernel, dim3(grid), dim3(256), 0, st, dim3(1, 1, 1), a.x,
                                    static_cast<__half *>(a.x16), total8);
         if (e != cudaSuccess) return e;
-        if (!make_map(&map_x, a.x16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.n, a.k, BN, 64)) return cudaErrorInvalidValue;
-        map_w = map_x;  // unused by the packed-format kernels
-        raw_g = make_raw_map(&map_raw, a.w, a.m, a.rb, PL::P);
         pdl = true;
     }
     GemmParams p;
@@ -615,18 +747,23 @@ static cudaError_t launch_gemm_t(const GemmArgs &a, int num_sms, cudaStream_t st
     p.N = static_cast<int>(a.n);
     p.K = static_cast<int>(a.k);
     p.units = static_cast<int>((a.k + RK - 1) / RK);
-    p.raw_g = raw_g;
+    p.raw_g = 0;
     p.w_early = pdl ? 1 : 0;
-    const int64_t m_tiles = (a.m + BM - 1) / BM, n_tiles = (a.n + BN - 1) / BN;
-    p.splits = choose_splits(m_tiles * n_tiles, p.units, num_sms);
+    p.splits = 1;
+    p.x3d = 0;
     p.status = a.status;
     p.limit_ns = a.wait_limit_ns;
     p.debug_skip = a.debug_skip_first_b_load;
-
-    const dim3 grid(static_cast<unsigned>(m_tiles), static_cast<unsigned>(n_tiles), static_cast<unsigned>(p.splits));
-    const dim3 cluster(1, 1, static_cast<unsigned>(p.splits));
-    return launch_pdl(gemm_tc_kernel<F, BN>, grid, dim3(THREADS), PL::SMEM, st, cluster,
-                      map_x, map_w, map_raw, p);
+    if constexpr (F != QMM_F32) {
+        // two 128-row subtiles per CTA halve the X bytes per MMA; take them
+        // when they cover the SMs as well without more split-K (whose partial
+        // reduction costs more than the X traffic it saves)
+        const int64_t n_tiles = (a.n + BN - 1) / BN;
+        const int64_t t1 = (a.m + BM - 1) / BM * n_tiles, t2 = (a.m + 2 * BM - 1) / (2 * BM) * n_tiles;
+        const int s1 = choose_splits(t1, p.units, num_sms), s2 = choose_splits(t2, p.units, num_sms);
+        if (s2 <= s1 && t2 * s2 >= std::min<int64_t>(t1 * s1, num_sms)) return launch_sub<F, 2>(a, p, num_sms, st);
+    }
+    return launch_sub<F, 1>(a, p, num_sms, st);
 }
 
 cudaError_t launch_gemm_tc(const GemmArgs &a, int num_sms, cudaStream_t st) {

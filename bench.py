@@ -43,6 +43,26 @@ WORKLOAD = ("LFM2.5-350M 512-token prefill projections (ffn_gate 4608x1024, ffn_
             "conv_in 3072x1024, attn_out 1024x1024), W in f32/q4_0/q8_0, n=512")
 # nominal dense tensor-core rates (PFLOP/s): f16/bf16 2.25, tf32 1.1
 TF32_OVER_F16 = 1.1 / 2.25
+# DRAM bytes (read + write) per launch of the tensor-core GEMM kernel, the
+# mean over the step's 12 launches, from one ncu capture of this workload
+# (profiles/gemm_tc_kernel_step_dram_traffic.md).  It describes the kernel
+# sources it was taken on; if they change, the bench reports null.
+GEMM_TRAFFIC_SOURCES = ("gemv_dequant_gemm_gb300/csrc/gemm_tc.cu", "gemv_dequant_gemm_gb300/csrc/decode.cuh",
+                        "gemv_dequant_gemm_gb300/csrc/common.cuh")
+GEMM_TRAFFIC_SHA16 = "729b2e5f56fd4ec2"
+GEMM_TRAFFIC_BYTES = 9.066e6
+
+
+def _gemm_traffic():
+    import hashlib
+    h = hashlib.sha256()
+    try:
+        for f in GEMM_TRAFFIC_SOURCES:
+            with open(os.path.join(ROOT, f), "rb") as fh:
+                h.update(fh.read())
+    except OSError:
+        return None
+    return GEMM_TRAFFIC_BYTES if h.hexdigest()[:16] == GEMM_TRAFFIC_SHA16 else None
 
 
 def _peaks():
@@ -315,7 +335,8 @@ def run_ours(args):
     achieved = flops_step / tot_t / 1e12
     peak_mix = flops_step / ideal_t / 1e12
     roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak_mix, 1), "unit": "TFLOP/s",
-                "frac": round(achieved / peak_mix, 4), "traffic": None,
+                "frac": round(achieved / peak_mix, 4), "traffic": _gemm_traffic(),
+                "traffic_unit": "bytes per gemm_tc_kernel launch (DRAM read + write, ncu)",
                 "kernel": "qmm_gemm tensor-core path (x_to_f16 + gemm_tc); per-call event-timed durations",
                 "peak_source": f"{peak_src} bf16 dense {f16_tflops} TFLOP/s; tf32 = x{TF32_OVER_F16:.3f} nominal"}
 

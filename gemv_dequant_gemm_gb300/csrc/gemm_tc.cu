@@ -241,9 +241,12 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
     volatile int *abort = &ctl->abort;
-    // everything below may touch memory the previous kernel in the stream
-    // wrote; only the weight producer may skip ahead (see w_early)
-    if (!(warp == WARP_RAW && p.w_early)) griddep_wait();
+    // Everything below may touch memory the previous kernel in the stream
+    // wrote.  When that kernel is x_to_f16_kernel (w_early), it wrote only the
+    // f16 copy of X, which the X producer alone reads: the other roles go
+    // ahead (weights, decode, MMA on stages the X producer has released), and
+    // the epilogue's stores follow the X loads through the barriers anyway.
+    if (!p.w_early || warp == WARP_X) griddep_wait();
     if (threadIdx.x == 0) griddep_launch();
 
     if (warp == WARP_RAW) {
@@ -562,19 +565,40 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
     }
 }
 
-// X [n][k] f32 -> [n][k] f16, round to nearest even; k % 8 == 0.
-__global__ void __launch_bounds__(256) x_to_f16_kernel(const float *__restrict__ x, __half *__restrict__ x16,
-                                                       int64_t total8) {
+// X [n][k] f32 -> [n][k] f16, round to nearest even; k % 8 == 0.  At most
+// two CTAs per SM, so that the GEMM CTAs launched behind it fit next to them
+// and stage and decode their first weights while it runs; four 32-byte
+// chunks in flight per thread.
+constexpr int X16_THREADS = 256, X16_CTAS_PER_SM = 2;
+__device__ __forceinline__ void x16_chunk(const float *__restrict__ x, __half *__restrict__ x16, int64_t i) {
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(x) + 2 * i);
+    const float4 b = __ldg(reinterpret_cast<const float4 *>(x) + 2 * i + 1);
+    const __half2 h0 = __floats2half2_rn(a.x, a.y), h1 = __floats2half2_rn(a.z, a.w);
+    const __half2 h2 = __floats2half2_rn(b.x, b.y), h3 = __floats2half2_rn(b.z, b.w);
+    reinterpret_cast<uint4 *>(x16)[i] = make_uint4(h2_bits(h0), h2_bits(h1), h2_bits(h2), h2_bits(h3));
+}
+__global__ void __launch_bounds__(X16_THREADS) x_to_f16_kernel(const float *__restrict__ x, __half *__restrict__ x16,
+                                                               int64_t total8) {
     griddep_wait();    // X may come from the kernel before this one; X16 may still be read by it
     griddep_launch();  // the GEMM may start staging weights while this runs
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total8; i += stride) {
-        const float4 a = __ldg(reinterpret_cast<const float4 *>(x) + 2 * i);
-        const float4 b = __ldg(reinterpret_cast<const float4 *>(x) + 2 * i + 1);
-        const __half2 h0 = __floats2half2_rn(a.x, a.y), h1 = __floats2half2_rn(a.z, a.w);
-        const __half2 h2 = __floats2half2_rn(b.x, b.y), h3 = __floats2half2_rn(b.z, b.w);
-        reinterpret_cast<uint4 *>(x16)[i] = make_uint4(h2_bits(h0), h2_bits(h1), h2_bits(h2), h2_bits(h3));
+    int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < total8; i += 4 * stride) {
+        float4 a[4], b[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            a[u] = __ldg(reinterpret_cast<const float4 *>(x) + 2 * (i + u * stride));
+            b[u] = __ldg(reinterpret_cast<const float4 *>(x) + 2 * (i + u * stride) + 1);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const __half2 h0 = __floats2half2_rn(a[u].x, a[u].y), h1 = __floats2half2_rn(a[u].z, a[u].w);
+            const __half2 h2 = __floats2half2_rn(b[u].x, b[u].y), h3 = __floats2half2_rn(b[u].z, b[u].w);
+            reinterpret_cast<uint4 *>(x16)[i + u * stride] =
+                make_uint4(h2_bits(h0), h2_bits(h1), h2_bits(h2), h2_bits(h3));
+        }
     }
+    for (; i < total8; i += stride) x16_chunk(x, x16, i);
 }
 
 // ---------------------------------------------------------------------------
@@ -732,9 +756,10 @@ static cudaError_t launch_gemm_t(const GemmArgs &a, int num_sms, cudaStream_t st
     bool pdl = false;
     if (F != QMM_F32) {
         const int64_t total8 = a.n * a.k / 8;
-        const int64_t want = (total8 + 255) / 256;
-        const int grid = static_cast<int>(want < 8LL * num_sms ? want : 8LL * num_sms);
-        cudaError_t e = launch_pdl(x_to_f16_kernel, dim3(grid), dim3(256), 0, st, dim3(1, 1, 1), a.x,
+        const int64_t want = (total8 + X16_THREADS - 1) / X16_THREADS;
+        const int64_t cap = static_cast<int64_t>(X16_CTAS_PER_SM) * num_sms;
+        const int grid = static_cast<int>(want < cap ? want : cap);
+        cudaError_t e = launch_pdl(x_to_f16_kernel, dim3(grid), dim3(X16_THREADS), 0, st, dim3(1, 1, 1), a.x,
                                    static_cast<__half *>(a.x16), total8);
         if (e != cudaSuccess) return e;
         pdl = true;

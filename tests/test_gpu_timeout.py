@@ -17,9 +17,11 @@ from qmm_cases import TC_ABS, TC_REL, assert_close, dev, nan_filled, weights
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("fmt", ["q8_0", "f32"])
-def test_expired_wait_is_reported_and_the_context_survives(h, fmt):
-    m, k, n = 256, 512, 256
+# (256, 512, 256): split-K clusters; (512, 256, 128): one CTA per tile;
+# (38912, 256, 128): two 128-row subtiles per CTA; f32: tf32 with split-K
+@pytest.mark.parametrize("fmt,m,k,n", [("q8_0", 256, 512, 256), ("q4_0", 512, 256, 128), ("q4_0", 38912, 256, 128),
+                                       ("f32", 256, 512, 256)])
+def test_expired_wait_is_reported_and_the_context_survives(h, fmt, m, k, n):
     w, x = weights(fmt, m, k), synth.activations(n, k)
     wd, xd = dev(w), dev(x)
     ws_bytes = q.qmm_gemm_workspace_bytes(fmt, m, k, n)

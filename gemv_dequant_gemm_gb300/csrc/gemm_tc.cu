@@ -4,30 +4,36 @@
 // The product is the one cera 0.4.0 examples/wgpu_gemm_bench.rs benchmarks
 // (struct Shape; its mul_mat_reg_tile kernel decodes src0 blocks into shared
 // memory with per-format loaders).  Here one CTA owns a 128 (m) x BN (n)
-// output tile and a slice of k:
+// output tile -- or two 128-row subtiles sharing every X stage (SUB = 2) --
+// and a slice of k:
 //
-//   warp 0      raw-weight producer: the packed bytes of 256 k of all 128
-//               rows at a time into a ring of raw stages -- one 2-D TMA box
-//               per stage over the rows viewed as 16-byte aligned row groups
-//               (G rows when G*row_bytes is a multiple of 16), else per-row
-//               1-D bulk copies of 16-byte aligned supersets of each row;
+//   warp 0      raw-weight producer: the packed bytes of 256 k of all the
+//               CTA's rows at a time into a ring of raw stages -- one 2-D TMA
+//               box per stage over the rows viewed as 16-byte aligned row
+//               groups (G rows when G*row_bytes is a multiple of 16), else
+//               per-row 1-D bulk copies of 16-byte aligned supersets of each
+//               row;
 //   warp 1      TMEM allocation and the single MMA-issuing thread:
 //               tcgen05.mma.kind::f16, M=128, N=BN, K=16, sixteen per 256-wide
 //               k stage, A (decoded W) read from tensor memory, B (X) from
-//               shared memory, fp32 accumulators in BN TMEM columns;
-//               tcgen05.commit releases the stages it read;
-//   warp 2      X producer: 2-D TMA of the f16 copy of X ([BN x 64] boxes,
-//               128-byte swizzle, four per stage) -- X is rounded once to f16
-//               (round to nearest even) by x_to_f16_kernel, like the
-//               cvt.rn.f16.f32 converter of aprender-serve cublas_prefill/mod.rs;
+//               shared memory, fp32 accumulators in BN TMEM columns per
+//               subtile; tcgen05.commit releases the stages it read;
+//   warp 2      X producer: the f16 copy of X through TMA with the 128-byte
+//               swizzle -- one request per stage through a 3-D tensor map
+//               ([k atoms][rows][atom]) when k allows, else one 2-D box per
+//               128-byte k atom.  X is rounded once to f16 (round to nearest
+//               even) by x_to_f16_kernel, like the cvt.rn.f16.f32 converter of
+//               aprender-serve cublas_prefill/mod.rs;
 //   warps 3-10  decode: thread = one W row = one TMEM lane (a warp owns the
 //               lane quarter warp%4); the two warps of a quarter take the two
-//               128-wide halves of every 256-wide k stage, turn the row's raw
-//               bytes (raw stage in shared memory) into f16 and write them
-//               into a ring of three A slots in tensor memory with tcgen05.st.
-//               The decoded weights never touch shared memory or HBM, so the
-//               shared-memory bandwidth is left to the X stream and the raw
-//               bytes; then the same warps run the epilogue.
+//               128-wide halves of every 256-wide k stage (SUB = 2: the two
+//               subtiles), turn the row's raw bytes (raw stage in shared
+//               memory) into f16 and write them into a ring of A slots in
+//               tensor memory with tcgen05.st.  The decoded weights never
+//               touch shared memory or HBM, so the shared-memory bandwidth is
+//               left to the X stream and the raw bytes; then the same warps
+//               run the epilogue: tcgen05.ld, the tile into shared memory as
+//               [n][m], one TMA store.
 //
 // Stages are long on purpose: the issuing thread waits on mbarriers between
 // stages, and a wait that follows tcgen05.commit costs a few hundred cycles,

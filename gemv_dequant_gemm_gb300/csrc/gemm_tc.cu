@@ -237,6 +237,22 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
         prefetch_tensormap(&tmap_x);
         if (TF32) prefetch_tensormap(&tmap_w);
         if (!TF32 && p.raw_g > 0) prefetch_tensormap(&tmap_raw);
+        // weights that may be read before the kernel in front ends: the first
+        // ring of raw stages goes out now, before the TMEM allocation and the
+        // block-wide barrier (this thread is the raw producer's issuing lane)
+        if constexpr (!TF32) {
+            const int npre = (p.w_early && p.raw_g > 0) ? min(RS, u1 - u0) : 0;
+            for (int i = 0; i < npre; ++i) {
+                const int64_t seg_off = static_cast<int64_t>(u0 + i) * PL::RB;
+                const int G = p.raw_g;
+                mbar_arrive_expect_tx(&ctl->raw_full[i], ROWS * PL::P);
+                for (int g = 0; g < G; ++g) {
+                    const int64_t xb = (static_cast<int64_t>(g) * p.rb + seg_off) & ~int64_t(15);
+                    tma_load_2d(sRaw + i * PL::RAW_STAGE + g * (ROWS / G) * PL::P, &tmap_raw,
+                                static_cast<int32_t>(xb / 2), m0 / G, &ctl->raw_full[i]);
+                }
+            }
+        }
     }
     if (warp == WARP_MMA) {
         tmem_alloc(&ctl->tmem_base, PL::TMEM_COLS);
@@ -261,9 +277,14 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
             int last[RS];
 #pragma unroll
             for (int r = 0; r < RS; ++r) last[r] = -1;
+            const int npre = (p.w_early && p.raw_g > 0) ? min(RS, u1 - u0) : 0;  // issued in the prologue
             for (int i = 0; u0 + i < u1; ++i) {
                 const int u = u0 + i, r = i % RS;
                 const uint32_t ph = (i / RS) & 1;
+                if (i < npre) {
+                    last[r] = i;
+                    continue;
+                }
                 const bool ok = mbar_wait_bounded(&ctl->raw_empty[r], ph ^ 1, abort, p.status, p.limit_ns);
                 if (!__all_sync(0xFFFFFFFFu, ok)) break;
                 const int64_t seg_off = static_cast<int64_t>(u) * PL::RB;

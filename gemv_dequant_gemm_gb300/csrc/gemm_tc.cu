@@ -269,7 +269,6 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
     // ahead (weights, decode, MMA on stages the X producer has released), and
     // the epilogue's stores follow the X loads through the barriers anyway.
     if (!p.w_early || warp == WARP_X) griddep_wait();
-    if (threadIdx.x == 0) griddep_launch();
 
     if (warp == WARP_RAW) {
         // ------------- raw weight producer (all 32 lanes) -------------
@@ -478,6 +477,9 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
     bool have = false;
     if (is_epi) {
         const bool drained = mbar_wait_drain(&ctl->accum, 0, p.status, p.limit_ns);
+        // the next kernel in the stream may launch now: its launch and start-up
+        // overlap this epilogue, and its CTAs do not sit waiting through the main loop
+        if (warp == WARP_DEC0 && lane == 0) griddep_launch();
         if (!drained) *abort = 1;
         have = __all_sync(0xFFFFFFFFu, drained && !*abort);  // tcgen05.ld is warp-collective
     }

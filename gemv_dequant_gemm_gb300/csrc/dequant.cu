@@ -7,6 +7,7 @@
 // the format's value rounded once to float32 (decode.cuh).
 #include "kernels.h"
 #include "decode.cuh"
+#include "l2hint.cuh"
 
 namespace qmm {
 
@@ -14,6 +15,16 @@ template <int F, typename Idx>
 __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict__ w, float *__restrict__ out,
                                                       Idx m, Idx k, Idx rb, float ts) {
     constexpr int QK = Fmt<F>::QK, BB = Fmt<F>::BB;
+    // an equal slice of the packed weights into L2 per CTA, before waiting
+    // for the kernel in front (a cache hint; the loads after the wait hit L2)
+    if (threadIdx.x == 0) {
+        const uint64_t wb = static_cast<uint64_t>(m) * static_cast<uint64_t>(rb);
+        const uint64_t chunk = (wb + gridDim.x - 1) / gridDim.x;
+        const uint64_t b0 = static_cast<uint64_t>(blockIdx.x) * chunk;
+        const uint64_t b1 = b0 + chunk < wb ? b0 + chunk : wb;
+        if (b0 < b1)
+            prefetch_l2_range(reinterpret_cast<uintptr_t>(w) + b0, reinterpret_cast<uintptr_t>(w) + b1);
+    }
     griddep_wait();
     griddep_launch();
     const Idx gpr = k / 8;  // groups per row

@@ -31,6 +31,7 @@
 #include <algorithm>
 
 #include "decode.cuh"
+#include "l2hint.cuh"
 #include "kernels.h"
 
 namespace qmm {
@@ -72,22 +73,14 @@ struct Ctl {
 }  // namespace gv
 
 // Warm L2 with this CTA's share of a plain GEMV's weights (its contiguous
-// stages) before waiting for the kernel in front: a cache hint, harmless even
-// if that kernel writes the range, so the weight stream that starts after the
-// wait reads from L2.  16-byte units (both ends rounded down), 64 KB requests.
+// stages) before waiting for the kernel in front, so the weight stream that
+// starts after the wait reads from L2.
 __device__ __forceinline__ void prefetch_own_rows_l2(const uint8_t *w, int64_t rb, int64_t rows, int64_t r0,
                                                      int64_t r1) {
     if (r1 > rows) r1 = rows;
     if (r0 >= r1) return;
     const uintptr_t base = reinterpret_cast<uintptr_t>(w);
-    const uintptr_t a0 = (base + static_cast<uintptr_t>(r0 * rb)) & ~uintptr_t(15);
-    const uintptr_t a1 = (base + static_cast<uintptr_t>(r1 * rb)) & ~uintptr_t(15);
-    for (uintptr_t a = a0; a < a1; a += 65536) {
-        const uintptr_t len = (a1 - a) < 65536 ? (a1 - a) : 65536;
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(static_cast<uint64_t>(a)),
-                     "r"(static_cast<uint32_t>(len))
-                     : "memory");
-    }
+    prefetch_l2_range(base + static_cast<uintptr_t>(r0 * rb), base + static_cast<uintptr_t>(r1 * rb));
 }
 
 // Wait with no early exit on abort, for copies already in flight.

@@ -73,6 +73,9 @@ def _load():
     lib.oracle_moe_gate_up.restype = ctypes.c_int
     lib.oracle_moe_gate_up.argtypes = [ctypes.c_int, P, P, P, I64, I64, ctypes.c_int, ctypes.c_int,
                                        I64, I64, P, P, ctypes.c_int]
+    lib.oracle_moe_down.restype = ctypes.c_int
+    lib.oracle_moe_down.argtypes = [ctypes.c_int, P, P, P, I64, I64, ctypes.c_int, ctypes.c_int,
+                                    I64, I64, P, P, ctypes.c_int]
     lib.oracle_max_threads.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     _lib = lib
@@ -205,4 +208,27 @@ def moe_gate_up(fmt: str, mats, scales, x, in_f: int, n_ff: int, n_used: int, t:
                                     row0, nrows, _ptr(y), _ptr(am), threads)
     if rc:
         raise ValueError(f"oracle_moe_gate_up failed ({rc})")
+    return y, am
+
+
+def moe_down(fmt: str, mats, scales, h, n_ff: int, gin: int, n_used: int, t: int,
+             row0: int = 0, nrows: int | None = None, threads: int = 0):
+    """(y, absmag), f64 [t][gin]: y[i][r] = sum over the token's pairs j =
+    i*n_used + u of scales[j] * (W_j[r] . h[j]); mats is a list of t*n_used
+    packed [gin][n_ff] matrices, h is [t*n_used][n_ff].  Rows outside
+    [row0, row0+nrows) are NaN."""
+    n_pairs = t * n_used
+    if len(mats) != n_pairs:
+        raise ValueError("need t*n_used matrices")
+    nrows = gin if nrows is None else nrows
+    keep = [_wbytes(a) for a in mats]
+    table = np.array([_ptr(a) for a in keep], dtype=np.uint64)
+    sc = np.ascontiguousarray(scales, dtype=np.float32)
+    ha = np.ascontiguousarray(h, dtype=np.float32).reshape(-1)
+    y = np.full((t, gin), np.nan)
+    am = np.full((t, gin), np.nan)
+    rc = _load().oracle_moe_down(_fmt(fmt), _ptr(table), _ptr(sc), _ptr(ha), n_ff, gin, n_used, t,
+                                 row0, nrows, _ptr(y), _ptr(am), threads)
+    if rc:
+        raise ValueError(f"oracle_moe_down failed ({rc})")
     return y, am

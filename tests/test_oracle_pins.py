@@ -314,3 +314,79 @@ def test_moe_matches_per_matrix_products():
             assert np.allclose(y[p, j], want, rtol=1e-13, atol=1e-12)
     # distinct matrices give distinct outputs (each pair reads its own matrix)
     assert not np.allclose(y[0, 0], y[0, 1])
+
+
+# ---- MoE down projection -----------------------------------------------------
+
+_E2M1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]  # OCP E2M1 magnitudes, codes 0-7; code | 8 negates
+
+
+def test_moe_down_all_ones_weights_sum_h():
+    # Every scale byte 0x38 (1.0) and every code 2 (1.0): W_j is all ones, so
+    # y[i][r] = sum_u scales[j] * sum(h[j]) with j = i*n_used + u.
+    n_ff, gin, n_used, t = 128, 4, 3, 2
+    n_pairs = t * n_used
+    grp = bytes([0x38] * 4 + [0x22] * 32)
+    mat = np.frombuffer(grp * (gin * n_ff // 64), np.uint8)
+    scales = np.array([0.5 + 0.01 * j for j in range(n_pairs)], np.float32)
+    h = (np.arange(n_pairs * n_ff, dtype=np.float32).reshape(n_pairs, n_ff) - 300) / 64
+    y, am = oracle.moe_down("nvfp4", [mat] * n_pairs, scales, h, n_ff, gin, n_used, t)
+    hs = h.astype(np.float64).sum(axis=1)
+    for i in range(t):
+        want = sum(float(scales[i * n_used + u]) * hs[i * n_used + u] for u in range(n_used))
+        assert np.allclose(y[i], want, rtol=1e-15, atol=0)
+        want_am = sum(abs(float(scales[i * n_used + u])) * np.abs(h[i * n_used + u].astype(np.float64)).sum()
+                      for u in range(n_used))
+        assert np.allclose(am[i], want_am, rtol=1e-15, atol=0)
+
+
+def test_moe_down_matches_hand_decoded_codes():
+    # Rows whose 64-weight groups cycle through all 16 E2M1 codes with E4M3
+    # scales 1.0 / 2.0 (0x38 / 0x40): the expected product comes from the OCP
+    # table above, not from the oracle's decoder.
+    n_ff, gin, n_used, t = 64, 3, 2, 1
+    rng = np.random.default_rng(9)
+    mats, wvals = [], []
+    for j in range(n_used):
+        rows = []
+        wj = np.zeros((gin, n_ff))
+        for r in range(gin):
+            sc = [0x38, 0x40, 0x38, 0x40]
+            codes = rng.integers(0, 16, n_ff)
+            packed = bytes(int(codes[2 * b]) | (int(codes[2 * b + 1]) << 4) for b in range(32))
+            rows.append(bytes(sc) + packed)
+            for c in range(n_ff):
+                mag = _E2M1[codes[c] & 7] * (-1.0 if codes[c] & 8 else 1.0)
+                wj[r, c] = mag * (1.0 if sc[c // 16] == 0x38 else 2.0)
+        mats.append(np.frombuffer(b"".join(rows), np.uint8))
+        wvals.append(wj)
+    scales = np.array([0.75, -1.25], np.float32)
+    h = rng.integers(-16, 17, (n_used, n_ff)).astype(np.float32) / 8
+    y, _ = oracle.moe_down("nvfp4", mats, scales, h, n_ff, gin, n_used, t)
+    want = sum(float(scales[u]) * (wvals[u] @ h[u].astype(np.float64)) for u in range(n_used))
+    assert np.array_equal(y[0], want)  # every product and partial sum is exact in f64
+
+
+def test_moe_down_pair_order_linearity_and_token_separation():
+    import synth
+    n_ff, gin, n_used, t = 128, 8, 3, 2
+    n_pairs = t * n_used
+    mats = [synth.nvfp4_rows(synth.nvfp4_matrix_seed(0, j, 2), gin, n_ff) for j in range(n_pairs)]
+    scales = np.array([0.5 + 0.01 * j for j in range(n_pairs)], np.float32)
+    h = synth.activations(n_pairs, n_ff)
+    y, _ = oracle.moe_down("nvfp4", mats, scales, h, n_ff, gin, n_used, t)
+    # reversing the pairs of token 1 (matrix, scale and activation together) leaves y unchanged
+    perm = [0, 1, 2, 5, 4, 3]
+    y2, _ = oracle.moe_down("nvfp4", [mats[p] for p in perm], scales[perm], h[perm], n_ff, gin, n_used, t)
+    assert np.allclose(y2, y, rtol=1e-13, atol=1e-12)
+    # y is linear in the pair scales
+    y3, _ = oracle.moe_down("nvfp4", mats, 2 * scales, h, n_ff, gin, n_used, t)
+    assert np.allclose(y3, 2 * y, rtol=1e-13, atol=1e-12)
+    # token 1's activations do not reach token 0's output
+    h4 = h.copy()
+    h4[n_used:] = 0
+    y4, _ = oracle.moe_down("nvfp4", mats, scales, h4, n_ff, gin, n_used, t)
+    assert np.array_equal(y4[0], y[0]) and np.all(y4[1] == 0)
+    # each pair uses its own matrix: swapping two matrices of token 0 changes y[0]
+    y5, _ = oracle.moe_down("nvfp4", [mats[1], mats[0]] + mats[2:], scales, h, n_ff, gin, n_used, t)
+    assert not np.allclose(y5[0], y[0])

@@ -424,7 +424,7 @@ def _time_calls(torch, stream, calls, reps):
 
 def run_sub_benches(q, lib, h, torch, synth, stream, hbm_gbs):
     sptr = stream.cuda_stream
-    out = {"gemv": [], "moe": None, "dequant": []}
+    out = {"gemv": [], "moe": None, "moe_down": None, "dequant": []}
     # GEMV: rotate over enough weight copies to exceed L2 several times
     for fmt in ("q4_k", "q8_0"):
         for m, k in ((4608, 1024), (1024, 4608)):
@@ -466,6 +466,31 @@ def run_sub_benches(q, lib, h, torch, synth, stream, hbm_gbs):
     gbs = wbytes / (ms * 1e-3) / 1e9
     out["moe"] = {"us": round(ms * 1e3, 3), "weight_bytes": wbytes, "weight_gbs": round(gbs, 1),
                   "frac_hbm": round(gbs / hbm_gbs, 4)}
+    del keep, tables
+    # MoE down projection: 8 experts of [gin 4096][n_ff 2048], per-pair
+    # activations, pairs summed into y; 6 rotated copies of the weight set
+    gin, n_ff_d = 4096, 2048
+    rb = q.qmm_row_bytes("nvfp4", n_ff_d)
+    keep, tables = [], []
+    for c in range(6):
+        ptrs = []
+        for j in range(n_pairs):
+            t = torch.from_numpy(synth.nvfp4_rows(synth.nvfp4_matrix_seed(c, j, 2), gin, n_ff_d)).cuda()
+            keep.append(t)
+            ptrs.append(t.data_ptr())
+        tables.append(torch.tensor(ptrs, dtype=torch.int64, device="cuda"))
+    hact = torch.from_numpy(synth.activations(n_pairs, n_ff_d, seed=1234)).cuda()
+    yd = torch.empty(1, gin, dtype=torch.float32, device="cuda")
+    wsb = q.qmm_moe_down_workspace_bytes(gin, n_used, 1)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    calls = [(lambda tb=tb: lib.qmm_moe_down(h, q.NVFP4, tb.data_ptr(), scales.data_ptr(), hact.data_ptr(),
+                                             yd.data_ptr(), n_ff_d, gin, n_used, 1, ws.data_ptr(), wsb, sptr))
+             for tb in tables]
+    ms = _time_calls(torch, stream, calls, 48)
+    wbytes = n_pairs * gin * rb
+    gbs = wbytes / (ms * 1e-3) / 1e9
+    out["moe_down"] = {"us": round(ms * 1e3, 3), "weight_bytes": wbytes, "weight_gbs": round(gbs, 1),
+                       "frac_hbm": round(gbs / hbm_gbs, 4), "launches_per_call": 2}
     del keep, tables
     # dequant: read packed + write f32
     for fmt, m, k in (("q4_k", 4608, 1024), ("q6_k", 4608, 1024), ("nvfp4", 2048, 4096)):

@@ -6,8 +6,9 @@ status codes into exceptions.  There is no fallback: if the library cannot be
 loaded, importing the functions raises.
 
 Names follow the C ABI: ``qmm_create``, ``qmm_destroy``, ``qmm_gemm``,
-``qmm_gemv``, ``qmm_moe_gemv``, ``qmm_dequant``, ``qmm_sync_status``,
-``qmm_row_bytes``, ``qmm_gemm_workspace_bytes``, ``qmm_strerror``.
+``qmm_gemv``, ``qmm_moe_gemv``, ``qmm_moe_down``, ``qmm_dequant``, ``qmm_sync_status``,
+``qmm_row_bytes``, ``qmm_gemm_workspace_bytes``, ``qmm_moe_down_workspace_bytes``,
+``qmm_strerror``.
 """
 from __future__ import annotations
 
@@ -29,6 +30,7 @@ STATUS = {0: "QMM_OK", 1: "QMM_ERR_INVALID_ARG", 2: "QMM_ERR_UNSUPPORTED", 3: "Q
 # Every symbol include/qmm.h and include/qmm_testing.h declare.
 EXPORTS = ("qmm_create", "qmm_destroy", "qmm_strerror", "qmm_block_weights", "qmm_block_bytes",
            "qmm_row_bytes", "qmm_gemm_workspace_bytes", "qmm_gemm", "qmm_gemv", "qmm_moe_gemv",
+           "qmm_moe_down_workspace_bytes", "qmm_moe_down",
            "qmm_dequant", "qmm_sync_status", "qmm_gemm_noalloc", "qmm_testing_set_wait_limit_ns",
            "qmm_testing_skip_first_stage_load")
 
@@ -65,6 +67,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "qmm_gemm": (I, [P, I, P, P, P, I64, I64, I64, P, SZ, P]),
         "qmm_gemv": (I, [P, I, P, P, P, I64, I64, I64, P]),
         "qmm_moe_gemv": (I, [P, I, P, P, P, P, I64, I64, I, I, P]),
+        "qmm_moe_down_workspace_bytes": (SZ, [I64, I, I]),
+        "qmm_moe_down": (I, [P, I, P, P, P, P, I64, I64, I, I, P, SZ, P]),
         "qmm_dequant": (I, [P, I, P, P, I64, I64, ctypes.c_float, P]),
         "qmm_sync_status": (I, [P, P]),
         "qmm_gemm_noalloc": (I, [I, P, P, P, I64, I64, I64, P]),
@@ -159,6 +163,18 @@ def qmm_gemv(h, t, w, x, dst, m, k, n, stream=None) -> None:
 def qmm_moe_gemv(h, t, w_ptrs, scales, x, y, in_f, n_ff, n_used, t_tokens, stream=None) -> None:
     _check(load().qmm_moe_gemv(h, _dt(t), _ptr(w_ptrs), _ptr(scales), _ptr(x), _ptr(y), in_f, n_ff, n_used,
                                t_tokens, _stream(stream)), "qmm_moe_gemv")
+
+
+def qmm_moe_down_workspace_bytes(gin: int, n_used: int, t_tokens: int) -> int:
+    return load().qmm_moe_down_workspace_bytes(gin, n_used, t_tokens)
+
+
+def qmm_moe_down(h, t, w_ptrs, scales, hact, y, n_ff, gin, n_used, t_tokens, workspace=None, workspace_bytes=None,
+                 stream=None) -> None:
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None or isinstance(workspace, int) else workspace.numel() * workspace.element_size()
+    _check(load().qmm_moe_down(h, _dt(t), _ptr(w_ptrs), _ptr(scales), _ptr(hact), _ptr(y), n_ff, gin, n_used,
+                               t_tokens, _ptr(workspace), workspace_bytes, _stream(stream)), "qmm_moe_down")
 
 
 def qmm_dequant(h, t, w, out, m, k, tensor_scale=1.0, stream=None) -> None:

@@ -220,6 +220,44 @@ int qmm_moe_gemv(qmm_handle h, qmm_dtype t, const void *const *w_ptrs, const flo
     });
 }
 
+size_t qmm_moe_down_workspace_bytes(int64_t gin, int n_used, int t_tokens) {
+    if (gin < 1 || n_used <= 1 || t_tokens < 1) return 0;
+    const size_t b = static_cast<size_t>(n_used) * static_cast<size_t>(t_tokens) * static_cast<size_t>(gin) * 4u;
+    return (b + 255u) & ~size_t(255);
+}
+
+int qmm_moe_down(qmm_handle h, qmm_dtype t, const void *const *w_ptrs, const float *scales, const float *hact,
+                 float *y, int64_t n_ff, int64_t gin, int n_used, int t_tokens, void *workspace,
+                 size_t workspace_bytes, void *stream) {
+    if (!valid_handle(h) || !known_dtype(t) || !w_ptrs || !scales || !hact || !y) return QMM_ERR_INVALID_ARG;
+    if (n_used < 1 || t_tokens < 1 || static_cast<int64_t>(n_used) * t_tokens > 4096) return QMM_ERR_SHAPE;
+    if (gin < 1 || gin > kMaxMN || n_ff < 1 || n_ff > kMaxK || qmm_row_bytes(t, n_ff) == 0) return QMM_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(w_ptrs) & 7u) != 0 || (reinterpret_cast<uintptr_t>(scales) & 3u) != 0 ||
+        !aligned16(hact) || !aligned16(y))
+        return QMM_ERR_ALIGN;
+    const int n_pairs = n_used * t_tokens;
+    const size_t ybytes = static_cast<size_t>(t_tokens) * gin * sizeof(float);
+    const size_t hbytes = static_cast<size_t>(n_pairs) * n_ff * sizeof(float);
+    const size_t sbytes = static_cast<size_t>(n_pairs) * sizeof(float);
+    const size_t pbytes = static_cast<size_t>(n_pairs) * sizeof(void *);
+    if (overlaps(y, ybytes, hact, hbytes) || overlaps(y, ybytes, scales, sbytes) || overlaps(y, ybytes, w_ptrs, pbytes))
+        return QMM_ERR_OVERLAP;
+    const size_t need = qmm_moe_down_workspace_bytes(gin, n_used, t_tokens);
+    if (need) {
+        if (!workspace || workspace_bytes < need) return QMM_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return QMM_ERR_ALIGN;
+        if (overlaps(workspace, need, y, ybytes) || overlaps(workspace, need, hact, hbytes) ||
+            overlaps(workspace, need, scales, sbytes) || overlaps(workspace, need, w_ptrs, pbytes))
+            return QMM_ERR_OVERLAP;
+    }
+    const int64_t rb = qmm_row_bytes(t, n_ff);
+    return on_device(h, [&] {
+        return qmm::launch_moe_down(t, w_ptrs, rb, scales, hact, y, static_cast<float *>(workspace), n_ff, gin,
+                                    n_used, t_tokens, h->num_sms, h->d_status, h->wait_limit_ns,
+                                    static_cast<cudaStream_t>(stream));
+    });
+}
+
 int qmm_dequant(qmm_handle h, qmm_dtype t, const void *w, float *out, int64_t m, int64_t k, float tensor_scale,
                 void *stream) {
     if (!valid_handle(h) || !known_dtype(t) || !w || !out) return QMM_ERR_INVALID_ARG;

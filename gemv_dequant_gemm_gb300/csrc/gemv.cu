@@ -8,6 +8,10 @@
 // 0.128.0 moe_rows_ceiling_bench.rs: the same product over a device table of
 // 2*n_pairs (plane, pair) matrices, each scaled by its own fp32 factor.
 //
+// The MoE down projection runs the same kernel with one matrix per (token,
+// expert) pair, each pair multiplying its own activation row, and a small
+// combine kernel sums each token's pairs in a fixed order.
+//
 // Design: the rows of all matrices are cut into stages of RT consecutive
 // rows.  A stage's packed bytes are contiguous in memory, so one producer
 // thread moves each stage into a shared-memory ring with a single 1-D bulk
@@ -1079,6 +1083,71 @@ cudaError_t launch_moe_gemv(int dtype, const void *const *w_ptrs, int64_t rb, co
     p.limit_ns = limit_ns;
     plan_stages(p, static_cast<int64_t>(tokens) * in_f * 4, gv::SMEM_BUDGET / 2);
     return dispatch_any(dtype, rx_params(p), p, 1, num_sms, st);
+}
+
+// MoE down projection, combine step: y[i][r] = sum over u < n_used of
+// part[i*n_used + u][r], summed in the order u = 0, 1, ... (deterministic).
+// Four consecutive r per thread when gin % 4 == 0 (16-byte loads and stores).
+__global__ void __launch_bounds__(256) moe_combine_kernel(const float *__restrict__ part, float *__restrict__ y,
+                                                          int64_t gin, int n_used, int64_t t) {
+    griddep_wait();
+    griddep_launch();
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    if ((gin & 3) == 0) {
+        const int64_t g4 = gin / 4, total = t * g4;
+        for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total; e += stride) {
+            const int64_t i = e / g4, c = e - i * g4;
+            const float4 *src = reinterpret_cast<const float4 *>(part) + i * n_used * g4 + c;
+            float4 a = src[0];
+            for (int u = 1; u < n_used; ++u) {
+                const float4 b = src[u * g4];
+                a.x += b.x;
+                a.y += b.y;
+                a.z += b.z;
+                a.w += b.w;
+            }
+            reinterpret_cast<float4 *>(y)[e] = a;
+        }
+    } else {
+        const int64_t total = t * gin;
+        for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total; e += stride) {
+            const int64_t i = e / gin, r = e - i * gin;
+            const float *src = part + i * n_used * gin + r;
+            float a = src[0];
+            for (int u = 1; u < n_used; ++u) a += src[u * gin];
+            y[e] = a;
+        }
+    }
+}
+
+cudaError_t launch_moe_down(int dtype, const void *const *w_ptrs, int64_t rb, const float *scales, const float *h,
+                            float *y, float *part, int64_t n_ff, int64_t gin, int n_used, int tokens, int num_sms,
+                            uint32_t *status, uint64_t limit_ns, cudaStream_t st) {
+    // the pair products: the MoE GEMV with one matrix per pair, each pair its
+    // own activation row (n_used = 1 makes the activation row the pair index)
+    const int n_pairs = n_used * tokens;
+    gv::Params p = {};
+    p.w_ptrs = w_ptrs;
+    p.scales = scales;
+    p.x = h;
+    p.dst = n_used == 1 ? y : part;
+    p.k = n_ff;
+    p.rb = rb;
+    p.rows_per_mat = static_cast<int>(gin);
+    p.mats = n_pairs;
+    p.n_pairs = n_pairs;
+    p.n_used = 1;
+    p.tokens = n_pairs;
+    p.status = status;
+    p.limit_ns = limit_ns;
+    plan_stages(p, static_cast<int64_t>(n_pairs) * n_ff * 4, gv::SMEM_BUDGET / 2);
+    cudaError_t e = dispatch_any(dtype, rx_params(p), p, 1, num_sms, st);
+    if (e != cudaSuccess || n_used == 1) return e;
+    const int64_t per = (gin & 3) == 0 ? gin / 4 : gin;
+    const int64_t want = (tokens * per + 255) / 256;
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, 4LL * num_sms)));
+    return launch_pdl(moe_combine_kernel, dim3(grid), dim3(256), 0, st, dim3(1, 1, 1),
+                      static_cast<const float *>(part), y, gin, n_used, static_cast<int64_t>(tokens));
 }
 
 }  // namespace qmm

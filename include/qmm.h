@@ -167,6 +167,36 @@ int qmm_moe_gemv(qmm_handle h, qmm_dtype t, const void *const *w_ptrs, const flo
                  const float *x, float *y, int64_t in_f, int64_t n_ff, int n_used, int t_tokens,
                  void *stream);
 
+/* MoE down projection over routed experts (memra-engine 0.128.0
+ * src/bin/moe_rows_ceiling_bench.rs: the down step after gate/up, one
+ * [gin][n_ff] matrix per pair at ptrs[2*n_pairs + j] of that page's table,
+ * the pairs of a token accumulated into y).  With n_pairs = t_tokens * n_used
+ * and pair j = i*n_used + u of token i:
+ *   y[i][r] = sum over u < n_used of scales[j] * sum_c W_j[r][c] * hact[j][c]
+ * for r < gin, where W_j = w_ptrs[j] is a [gin][n_ff] packed matrix and
+ * hact[j] is that pair's n_ff activations (the gated gate/up output).
+ *   - w_ptrs: DEVICE array of n_pairs device pointers (pass table + 2*n_pairs
+ *     for a gate/up/down table laid out as that page's), each 16-byte
+ *     aligned; a NULL or misaligned entry makes its token's rows NaN and
+ *     latches QMM_ERR_ALIGN for qmm_sync_status.
+ *   - scales: device float[n_pairs], the factor of each pair (its routing
+ *     weight, a per-matrix scale, or their product: the call only multiplies).
+ *   - hact: device float32 [n_pairs][n_ff]; y: device float32 [t_tokens][gin],
+ *     overwritten (not accumulated into).
+ *   - workspace: device scratch of qmm_moe_down_workspace_bytes(gin, n_used,
+ *     t_tokens) bytes (0 when n_used == 1: then pass NULL), 16-byte aligned,
+ *     overlapping no other argument; it holds the per-pair products, which a
+ *     second kernel sums per token in the order u = 0, 1, ... so results are
+ *     deterministic.
+ * Any dtype; fp32 decode and FMA; accuracy |y - exact| <= 1e-5 *
+ * sum_u |scales[j]| * sum_c |W_j * hact_j|.  Sizes: 1 <= n_used, t_tokens;
+ * n_pairs <= 4096; 1 <= gin <= 2^24; n_ff % QK == 0.  Errors as qmm_moe_gemv,
+ * and QMM_ERR_WORKSPACE (workspace missing or too small). */
+size_t qmm_moe_down_workspace_bytes(int64_t gin, int n_used, int t_tokens);
+int qmm_moe_down(qmm_handle h, qmm_dtype t, const void *const *w_ptrs, const float *scales,
+                 const float *hact, float *y, int64_t n_ff, int64_t gin, int n_used, int t_tokens,
+                 void *workspace, size_t workspace_bytes, void *stream);
+
 /* Standalone dequant (aprender-serve cublas_prefill/mod.rs module doc, v1
  * path, which dequantizes Q4K/Q6K weights into an FP32 scratch buffer):
  * out[m][k] float32 = the decoded

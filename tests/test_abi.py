@@ -47,6 +47,10 @@ def test_workspace_bytes():
     assert q.qmm_gemm_workspace_bytes("q4_0", 64, 32, 9) == 768  # 576 rounded up to 256
     assert q.qmm_gemm_workspace_bytes("q8_0", 64, 64, 8) == 0    # GEMV regime
     assert q.qmm_gemm_workspace_bytes("f32", 64, 64, 512) == 0   # tf32 path reads X directly
+    assert q.qmm_moe_down_workspace_bytes(4096, 8, 1) == 8 * 4096 * 4
+    assert q.qmm_moe_down_workspace_bytes(101, 3, 2) == 2560     # 2424 rounded up to 256
+    assert q.qmm_moe_down_workspace_bytes(4096, 1, 5) == 0       # one expert: products go straight to y
+    assert q.qmm_moe_down_workspace_bytes(0, 8, 1) == 0
 
 
 def test_strerror_covers_every_status():
@@ -62,6 +66,7 @@ def test_null_handle_and_arguments_are_rejected_without_a_device():
     assert lib.qmm_gemv(None, 1, 16, 16, 16, 32, 32, 1, None) == 1
     assert lib.qmm_dequant(None, 1, 16, 16, 32, 32, 1.0, None) == 1
     assert lib.qmm_moe_gemv(None, 5, 16, 16, 16, 16, 64, 16, 1, 1, None) == 1
+    assert lib.qmm_moe_down(None, 5, 16, 16, 16, 16, 64, 16, 2, 1, 16, 256, None) == 1
     assert lib.qmm_sync_status(None, None) == 1
     assert lib.qmm_destroy(None) == 0
     assert lib.qmm_create(0, None) == 1

@@ -595,27 +595,42 @@ __device__ __forceinline__ uint32_t lds32(uint32_t a) {
     return v;
 }
 
+// Two E2M1 codes of one byte as an exact f32 pair (element of the low nibble
+// first): the hardware E2M1 -> f16x2 conversion, then f16 -> f32 widening,
+// both exact for every code.
+__device__ __forceinline__ uint64_t f16x2_to_f2(uint32_t h) {
+    uint64_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\t.reg .f32 a, b;\n\t"
+        "mov.b32 {lo, hi}, %1;\n\t"
+        "cvt.f32.f16 a, lo;\n\t"
+        "cvt.f32.f16 b, hi;\n\t"
+        "mov.b64 %0, {a, b};\n\t}"
+        : "=l"(r) : "r"(h));
+    return r;
+}
+__device__ __forceinline__ void e2m1x8_to_f2(uint32_t c, uint64_t *w) {
+    uint32_t h0, h1, h2, h3;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3) : "r"(c));
+    w[0] = f16x2_to_f2(h0);
+    w[1] = f16x2_to_f2(h1);
+    w[2] = f16x2_to_f2(h2);
+    w[3] = f16x2_to_f2(h3);
+}
+
 // 16 NVFP4 weights of one scale region (codes at shared address `codes`,
-// scale byte at `scb`) as 8 f32 pairs holding twice the e2m1 values: the bytes
-// 2*value + 12 become (2^23 + byte) by byte permutation and one f32x2
-// subtraction leaves 2*value exactly.  *scale receives the e4m3 scale.
+// scale byte at `scb`) as 8 exact f32 pairs of their E2M1 values; *scale
+// receives the e4m3 scale.
 __device__ __forceinline__ void nvfp4_unit16(uint32_t codes, uint32_t scb, uint64_t (&w2)[8], float &scale) {
     const uint32_t c0 = lds32(codes), c1 = lds32(codes + 4);
     scale = e4m3_to_f32(lds8(scb));
-    const uint32_t n0 = c0 ^ 0x88888888u, n1 = c1 ^ 0x88888888u;
-    const uint32_t b[4] = {
-        prmt_signed(0x0F0E0D0Cu, 0x18141210u, c0) | prmt_signed(0x090A0B0Cu, 0x00040608u, n0),
-        prmt_signed(0x0F0E0D0Cu, 0x18141210u, c0 >> 16) | prmt_signed(0x090A0B0Cu, 0x00040608u, n0 >> 16),
-        prmt_signed(0x0F0E0D0Cu, 0x18141210u, c1) | prmt_signed(0x090A0B0Cu, 0x00040608u, n1),
-        prmt_signed(0x0F0E0D0Cu, 0x18141210u, c1 >> 16) | prmt_signed(0x090A0B0Cu, 0x00040608u, n1 >> 16)};
-    const uint64_t minus = f2_pack(-8388620.0f, -8388620.0f);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        w2[2 * q] = f2_add(f2_pack(__uint_as_float(__byte_perm(b[q], 0x4B000000u, 0x7440u)),
-                                   __uint_as_float(__byte_perm(b[q], 0x4B000000u, 0x7441u))), minus);
-        w2[2 * q + 1] = f2_add(f2_pack(__uint_as_float(__byte_perm(b[q], 0x4B000000u, 0x7442u)),
-                                       __uint_as_float(__byte_perm(b[q], 0x4B000000u, 0x7443u))), minus);
-    }
+    e2m1x8_to_f2(c0, w2);
+    e2m1x8_to_f2(c1, w2 + 4);
 }
 
 // sum_i w2[i] . x2[i] over 8 pairs, two f32x2 chains.
@@ -778,7 +793,7 @@ __global__ void __launch_bounds__(gr::THREADS, 1) gemv_rx_kernel(const gr::Param
         const int team = tid / p.tk, tk = tid % p.tk;
         float xr[JM][NV][UW];
         float xs[JM][NV];  // per-unit sums of X (Q4_K minimum term)
-        uint64_t x2[JM][NV][8];  // NVFP4: X pairs halved (the codes decode to twice their value)
+        uint64_t x2[JM][NV][8];  // NVFP4: X as f32 pairs
         uint32_t scoff[JM], cdoff[JM];  // NVFP4: byte offsets of each unit's scale and codes in a row
         if constexpr (F == QMM_NVFP4) {
 #pragma unroll
@@ -812,7 +827,7 @@ __global__ void __launch_bounds__(gr::THREADS, 1) gemv_rx_kernel(const gr::Param
                         if constexpr (F == QMM_NVFP4) {
 #pragma unroll
                             for (int q = 0; q < 8; ++q)
-                                x2[jj][v][q] = f2_pack(0.5f * xr[jj][v][2 * q], 0.5f * xr[jj][v][2 * q + 1]);
+                                x2[jj][v][q] = f2_pack(xr[jj][v][2 * q], xr[jj][v][2 * q + 1]);
                         }
                     }
                 }

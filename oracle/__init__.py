@@ -21,7 +21,7 @@ _SRC = os.path.join(_HERE, "qmm_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 
 # The oracle's own format numbering (qmm_oracle.c, enum ORC_*).
-FORMATS = {"f32": 0, "q4_0": 1, "q8_0": 2, "q4_k": 3, "q6_k": 4, "nvfp4": 5}
+FORMATS = {"f32": 0, "q4_0": 1, "q8_0": 2, "q4_k": 3, "q6_k": 4, "nvfp4": 5, "nvfp4_v2": 6}
 
 _lib = None
 
@@ -76,6 +76,8 @@ def _load():
     lib.oracle_moe_down.restype = ctypes.c_int
     lib.oracle_moe_down.argtypes = [ctypes.c_int, P, P, P, I64, I64, ctypes.c_int, ctypes.c_int,
                                     I64, I64, P, P, ctypes.c_int]
+    lib.oracle_nvfp4_repack_v2.restype = ctypes.c_int
+    lib.oracle_nvfp4_repack_v2.argtypes = [P, P, I64, I64]
     lib.oracle_max_threads.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     _lib = lib
@@ -148,6 +150,18 @@ def decode(fmt: str, w, m: int, k: int) -> np.ndarray:
         rc = lib.oracle_decode_row(_fmt(fmt), _ptr(wb) + r * rb, k, _ptr(out) + r * k * 8)
         if rc:
             raise ValueError(f"decode failed ({rc})")
+    return out
+
+
+def nvfp4_repack_v2(v1, m: int, k: int) -> np.ndarray:
+    """NVFP4 36-byte-group rows -> V2 rows (codes, then the scale stream)."""
+    src = np.ascontiguousarray(np.asarray(v1, dtype=np.uint8).reshape(-1))
+    if src.size != m * row_bytes("nvfp4", k):
+        raise ValueError("v1 has the wrong size")
+    out = np.empty(m * row_bytes("nvfp4_v2", k), np.uint8)
+    rc = _load().oracle_nvfp4_repack_v2(_ptr(src), _ptr(out), m, k)
+    if rc != 0:
+        raise ValueError(f"oracle_nvfp4_repack_v2: status {rc}")
     return out
 
 

@@ -25,6 +25,9 @@
  *                bytes then 32 B of E2M1 nibbles
  *              - main: pointer table index plane*n_pairs + j, per-matrix scale
  *                scl[pr] = 0.5 + 0.01*pr, gate = plane 0, up = plane 1
+ *              - main, the V2 arms: the same values repacked "split" so that
+ *                each row holds 18 B per 32 weights (16 B of codes, 2 scale
+ *                bytes) with the scales as one contiguous stream
  *   [hrx]    hrx-rs patch_bench.rs, fn float: the binary16 decode with
  *              subnormals (exponent field 0 -> mantissa * 2^-24)
  *   [aprender] aprender-serve 0.70.2 cublas_prefill/mod.rs, module doc: its
@@ -50,7 +53,8 @@ enum {
     ORC_Q8_0 = 2,
     ORC_Q4_K = 3,
     ORC_Q6_K = 4,
-    ORC_NVFP4 = 5
+    ORC_NVFP4 = 5,
+    ORC_NVFP4_V2 = 6
 };
 
 /* ---------------------------------------------------------------------- */
@@ -121,6 +125,7 @@ int64_t oracle_block_weights(int fmt) {
     case ORC_Q4_K: return 256;
     case ORC_Q6_K: return 256;
     case ORC_NVFP4: return 64;
+    case ORC_NVFP4_V2: return 32;
     default: return 0;
     }
 }
@@ -134,6 +139,7 @@ int64_t oracle_block_bytes(int fmt) {
     case ORC_Q4_K: return 144;
     case ORC_Q6_K: return 210;
     case ORC_NVFP4: return 36;
+    case ORC_NVFP4_V2: return 18;
     default: return 0;
     }
 }
@@ -230,12 +236,30 @@ static void decode_nvfp4(const uint8_t *b, double *out) {
     }
 }
 
+/* NVFP4 V2 row of k weights ([memra] main, the V2 arms; the byte order is
+ * the reading that keeps each 32-weight code group on a 16-byte boundary):
+ * first the k/2 code bytes (the low nibble of byte j is element 2j, the high
+ * nibble element 2j+1, as in the 36-byte groups), then the k/16 E4M3 scale
+ * bytes, scale byte s covering elements 16s..16s+15.  Value e2m1 * e4m3. */
+static void decode_nvfp4_v2_row(const uint8_t *row, int64_t k, double *out) {
+    const uint8_t *scales = row + k / 2;
+    for (int64_t e = 0; e < k; ++e) {
+        uint8_t byte = row[e / 2];
+        uint32_t nib = (e % 2 == 0) ? (byte & 15u) : (byte >> 4);
+        out[e] = oracle_e2m1(nib) * oracle_e4m3(scales[e / 16]);
+    }
+}
+
 /* Decode one packed row of k weights into out[0..k).  Returns 0, or -1 for an
  * unknown format or a k that is not a whole number of blocks. */
 int oracle_decode_row(int fmt, const uint8_t *row, int64_t k, double *out) {
     int64_t qk = oracle_block_weights(fmt);
     int64_t bb = oracle_block_bytes(fmt);
     if (qk == 0 || k < 0 || k % qk != 0) return -1;
+    if (fmt == ORC_NVFP4_V2) {
+        decode_nvfp4_v2_row(row, k, out);
+        return 0;
+    }
     for (int64_t blk = 0; blk < k / qk; ++blk) {
         const uint8_t *b = row + blk * bb;
         double *o = out + blk * qk;
@@ -265,6 +289,29 @@ int64_t oracle_row_bytes(int fmt, int64_t k) {
 }
 
 /* ---------------------------------------------------------------------- */
+/* NVFP4 36-byte groups -> V2 rows ([memra] main: the V2 arms read the same    */
+/* values, repacked)                                                        */
+/* ---------------------------------------------------------------------- */
+
+/* v2[m][k/32*18] from v1[m][k/64*36]: for every row, group g's 32 code bytes
+ * go to bytes 32g..32g+31 of the row's code area and its 4 scale bytes to
+ * bytes 4g..4g+3 of the scale area that follows (at k/2).  Returns -1 unless
+ * k is a positive multiple of 64. */
+int oracle_nvfp4_repack_v2(const uint8_t *v1, uint8_t *v2, int64_t m, int64_t k) {
+    if (k <= 0 || k % 64 != 0 || m < 0) return -1;
+    int64_t rb1 = k / 64 * 36, rb2 = k / 32 * 18;
+    for (int64_t r = 0; r < m; ++r) {
+        const uint8_t *src = v1 + r * rb1;
+        uint8_t *dst = v2 + r * rb2;
+        for (int64_t g = 0; g < k / 64; ++g) {
+            for (int j = 0; j < 32; ++j) dst[32 * g + j] = src[36 * g + 4 + j];
+            for (int j = 0; j < 4; ++j) dst[k / 2 + 4 * g + j] = src[36 * g + j];
+        }
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
 /* Standalone dequant ([aprender] v1 path: packed weights -> FP32)          */
 /* ---------------------------------------------------------------------- */
 
@@ -284,7 +331,7 @@ int oracle_dequant(int fmt, const uint8_t *w, int64_t m, int64_t k, double tenso
         }
         for (int64_t c = 0; c < k; ++c) {
             double v = tmp[c];
-            if (fmt == ORC_NVFP4) v = v * tensor_scale;
+            if (fmt == ORC_NVFP4 || fmt == ORC_NVFP4_V2) v = v * tensor_scale;
             out[r * k + c] = (float)v;
         }
     }

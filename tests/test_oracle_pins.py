@@ -390,3 +390,51 @@ def test_moe_down_pair_order_linearity_and_token_separation():
     # each pair uses its own matrix: swapping two matrices of token 0 changes y[0]
     y5, _ = oracle.moe_down("nvfp4", [mats[1], mats[0]] + mats[2:], scales, h, n_ff, gin, n_used, t)
     assert not np.allclose(y5[0], y[0])
+
+
+# ---- NVFP4 V2 rows (codes, then the scale stream) ----------------------------
+
+_E4M3_BY_HAND = {0x38: 1.0, 0x40: 2.0, 0x30: 0.5, 0xB8: -1.0}  # sign | 4-bit exponent (bias 7) | 3-bit mantissa
+
+
+def test_nvfp4_v2_hand_decoded_row():
+    # k = 64: 32 code bytes, then 4 scale bytes; expected values from the OCP
+    # E2M1 table and the four E4M3 bytes decoded by hand above
+    k = 64
+    rng = np.random.default_rng(21)
+    codes = rng.integers(0, 16, k)
+    code_bytes = bytes(int(codes[2 * j]) | (int(codes[2 * j + 1]) << 4) for j in range(k // 2))
+    scale_bytes = bytes([0x38, 0x40, 0x30, 0xB8])
+    row = np.frombuffer(code_bytes + scale_bytes, np.uint8)
+    assert row.size == oracle.row_bytes("nvfp4_v2", k) == 36
+    got = oracle.decode("nvfp4_v2", row, 1, k)[0]
+    want = [(_E2M1[c & 7] * (-1.0 if c & 8 else 1.0)) * _E4M3_BY_HAND[scale_bytes[e // 16]]
+            for e, c in enumerate(codes)]
+    assert np.array_equal(got, np.array(want))
+
+
+def test_nvfp4_v2_row_sizes():
+    assert oracle.block_weights("nvfp4_v2") == 32 and oracle.block_bytes("nvfp4_v2") == 18
+    assert oracle.row_bytes("nvfp4_v2", 32) == 18
+    assert oracle.row_bytes("nvfp4_v2", 4096) == oracle.row_bytes("nvfp4", 4096) == 2304
+    assert oracle.row_bytes("nvfp4_v2", 48) == 0
+
+
+def test_nvfp4_repack_v2_is_the_split_of_the_groups():
+    import synth
+    m, k = 5, 256
+    v1 = synth.nvfp4_rows(0x5151, m, k)
+    v2 = oracle.nvfp4_repack_v2(v1, m, k)
+    # the same split restated with numpy reshapes: per row, every group's 32
+    # code bytes in group order, then every group's 4 scale bytes
+    grp = v1.reshape(m, k // 64, 36)
+    want = np.concatenate([grp[:, :, 4:].reshape(m, -1), grp[:, :, :4].reshape(m, -1)], axis=1).reshape(-1)
+    assert np.array_equal(v2, want)
+    # the V2 rows hold the same values
+    assert np.array_equal(oracle.decode("nvfp4_v2", v2, m, k), oracle.decode("nvfp4", v1, m, k))
+    x = synth.activations(3, k)
+    a, am = oracle.matmul("nvfp4", v1, x, m, k, 3)
+    b, bm = oracle.matmul("nvfp4_v2", v2, x, m, k, 3)
+    assert np.array_equal(a, b) and np.array_equal(am, bm)
+    with pytest.raises(ValueError):
+        oracle.nvfp4_repack_v2(v1[:36], 1, 32)  # k must be a multiple of 64

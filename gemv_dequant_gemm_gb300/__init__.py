@@ -6,7 +6,7 @@ status codes into exceptions.  There is no fallback: if the library cannot be
 loaded, importing the functions raises.
 
 Names follow the C ABI: ``qmm_create``, ``qmm_destroy``, ``qmm_gemm``,
-``qmm_gemv``, ``qmm_moe_gemv``, ``qmm_moe_down``, ``qmm_dequant``, ``qmm_sync_status``,
+``qmm_gemv``, ``qmm_moe_gemv``, ``qmm_moe_down``, ``qmm_nvfp4_repack_v2``, ``qmm_dequant``, ``qmm_sync_status``,
 ``qmm_row_bytes``, ``qmm_gemm_workspace_bytes``, ``qmm_moe_down_workspace_bytes``,
 ``qmm_strerror``.
 """
@@ -19,8 +19,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libqmm.so")
 
 # qmm_dtype values (include/qmm.h)
-F32, Q4_0, Q8_0, Q4_K, Q6_K, NVFP4 = 0, 1, 2, 3, 4, 5
-DTYPES = {"f32": F32, "q4_0": Q4_0, "q8_0": Q8_0, "q4_k": Q4_K, "q6_k": Q6_K, "nvfp4": NVFP4}
+F32, Q4_0, Q8_0, Q4_K, Q6_K, NVFP4, NVFP4_V2 = 0, 1, 2, 3, 4, 5, 6
+DTYPES = {"f32": F32, "q4_0": Q4_0, "q8_0": Q8_0, "q4_k": Q4_K, "q6_k": Q6_K, "nvfp4": NVFP4, "nvfp4_v2": NVFP4_V2}
 GEMV_MAX_N = 8
 
 STATUS = {0: "QMM_OK", 1: "QMM_ERR_INVALID_ARG", 2: "QMM_ERR_UNSUPPORTED", 3: "QMM_ERR_SHAPE",
@@ -30,7 +30,7 @@ STATUS = {0: "QMM_OK", 1: "QMM_ERR_INVALID_ARG", 2: "QMM_ERR_UNSUPPORTED", 3: "Q
 # Every symbol include/qmm.h and include/qmm_testing.h declare.
 EXPORTS = ("qmm_create", "qmm_destroy", "qmm_strerror", "qmm_block_weights", "qmm_block_bytes",
            "qmm_row_bytes", "qmm_gemm_workspace_bytes", "qmm_gemm", "qmm_gemv", "qmm_moe_gemv",
-           "qmm_moe_down_workspace_bytes", "qmm_moe_down",
+           "qmm_moe_down_workspace_bytes", "qmm_moe_down", "qmm_nvfp4_repack_v2",
            "qmm_dequant", "qmm_sync_status", "qmm_gemm_noalloc", "qmm_testing_set_wait_limit_ns",
            "qmm_testing_skip_first_stage_load")
 
@@ -70,6 +70,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "qmm_moe_down_workspace_bytes": (SZ, [I64, I, I]),
         "qmm_moe_down": (I, [P, I, P, P, P, P, I64, I64, I, I, P, SZ, P]),
         "qmm_dequant": (I, [P, I, P, P, I64, I64, ctypes.c_float, P]),
+        "qmm_nvfp4_repack_v2": (I, [P, P, P, I64, I64, P]),
         "qmm_sync_status": (I, [P, P]),
         "qmm_gemm_noalloc": (I, [I, P, P, P, I64, I64, I64, P]),
         "qmm_testing_set_wait_limit_ns": (I, [P, ctypes.c_uint64]),
@@ -175,6 +176,10 @@ def qmm_moe_down(h, t, w_ptrs, scales, hact, y, n_ff, gin, n_used, t_tokens, wor
         workspace_bytes = 0 if workspace is None or isinstance(workspace, int) else workspace.numel() * workspace.element_size()
     _check(load().qmm_moe_down(h, _dt(t), _ptr(w_ptrs), _ptr(scales), _ptr(hact), _ptr(y), n_ff, gin, n_used,
                                t_tokens, _ptr(workspace), workspace_bytes, _stream(stream)), "qmm_moe_down")
+
+
+def qmm_nvfp4_repack_v2(h, v1, v2, m, k, stream=None) -> None:
+    _check(load().qmm_nvfp4_repack_v2(h, _ptr(v1), _ptr(v2), m, k, _stream(stream)), "qmm_nvfp4_repack_v2")
 
 
 def qmm_dequant(h, t, w, out, m, k, tensor_scale=1.0, stream=None) -> None:

@@ -26,7 +26,13 @@ constexpr int64_t kMaxK = int64_t(1) << 20;
 
 bool valid_handle(qmm_handle h) { return h != nullptr && h->magic == kMagic; }
 
-bool known_dtype(int t) { return t >= QMM_F32 && t <= QMM_NVFP4; }
+bool known_dtype(int t) { return t >= QMM_F32 && t <= QMM_NVFP4_V2; }
+
+// k is a whole number of blocks; V2 rows also need k % 64 == 0, which keeps
+// every 4-byte code word of every row aligned.
+bool k_ok(qmm_dtype t, int64_t k) {
+    return qmm_row_bytes(t, k) != 0 && (t != QMM_NVFP4_V2 || k % 64 == 0);
+}
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -50,7 +56,7 @@ int check_product(qmm_handle h, qmm_dtype t, const void *w, const float *x, cons
                   int64_t n) {
     if (!valid_handle(h) || !known_dtype(t) || !w || !x || !dst) return QMM_ERR_INVALID_ARG;
     if (m < 1 || n < 1 || m > kMaxMN || n > kMaxMN || k < 1 || k > kMaxK) return QMM_ERR_SHAPE;
-    if (qmm_row_bytes(t, k) == 0) return QMM_ERR_SHAPE;
+    if (!k_ok(t, k)) return QMM_ERR_SHAPE;
     if (!aligned16(w) || !aligned16(x) || !aligned16(dst)) return QMM_ERR_ALIGN;
     const size_t wbytes = static_cast<size_t>(qmm_row_bytes(t, k) * m);
     const size_t dbytes = static_cast<size_t>(n * m) * sizeof(float);
@@ -87,6 +93,7 @@ int64_t qmm_block_weights(qmm_dtype t) {
     case QMM_Q4_K: return 256;
     case QMM_Q6_K: return 256;
     case QMM_NVFP4: return 64;
+    case QMM_NVFP4_V2: return 32;
     default: return 0;
     }
 }
@@ -99,6 +106,7 @@ int64_t qmm_block_bytes(qmm_dtype t) {
     case QMM_Q4_K: return 144;
     case QMM_Q6_K: return 210;
     case QMM_NVFP4: return 36;
+    case QMM_NVFP4_V2: return 18;
     default: return 0;
     }
 }
@@ -110,7 +118,7 @@ int64_t qmm_row_bytes(qmm_dtype t, int64_t k) {
 }
 
 size_t qmm_gemm_workspace_bytes(qmm_dtype t, int64_t /*m*/, int64_t k, int64_t n) {
-    if (!known_dtype(t) || t == QMM_F32 || n <= QMM_GEMV_MAX_N || k < 1 || n < 1) return 0;
+    if (!known_dtype(t) || t == QMM_F32 || t == QMM_NVFP4_V2 || n <= QMM_GEMV_MAX_N || k < 1 || n < 1) return 0;
     const size_t b = static_cast<size_t>(n) * static_cast<size_t>(k) * 2u;
     return (b + 255u) & ~size_t(255);
 }
@@ -173,6 +181,7 @@ int qmm_gemm(qmm_handle h, qmm_dtype t, const void *w, const float *x, float *ds
     int st = check_product(h, t, w, x, dst, m, k, n);
     if (st != QMM_OK) return st;
     if (n <= QMM_GEMV_MAX_N) return qmm_gemv(h, t, w, x, dst, m, k, n, stream);
+    if (t == QMM_NVFP4_V2) return QMM_ERR_UNSUPPORTED;  // the tensor-core decode reads 36-byte groups
     if (t == QMM_F32 && k % 4 != 0) return QMM_ERR_SHAPE;  // TMA row pitch must be a multiple of 16 bytes
     const size_t need = qmm_gemm_workspace_bytes(t, m, k, n);
     if (need) {
@@ -203,7 +212,7 @@ int qmm_moe_gemv(qmm_handle h, qmm_dtype t, const void *const *w_ptrs, const flo
                  int64_t in_f, int64_t n_ff, int n_used, int t_tokens, void *stream) {
     if (!valid_handle(h) || !known_dtype(t) || !w_ptrs || !scales || !x || !y) return QMM_ERR_INVALID_ARG;
     if (n_used < 1 || t_tokens < 1 || static_cast<int64_t>(n_used) * t_tokens > 4096) return QMM_ERR_SHAPE;
-    if (n_ff < 1 || n_ff > kMaxMN || in_f < 1 || in_f > kMaxK || qmm_row_bytes(t, in_f) == 0) return QMM_ERR_SHAPE;
+    if (n_ff < 1 || n_ff > kMaxMN || in_f < 1 || in_f > kMaxK || !k_ok(t, in_f)) return QMM_ERR_SHAPE;
     if ((reinterpret_cast<uintptr_t>(w_ptrs) & 7u) != 0 || (reinterpret_cast<uintptr_t>(scales) & 3u) != 0 ||
         !aligned16(x) || !aligned16(y))
         return QMM_ERR_ALIGN;
@@ -231,7 +240,7 @@ int qmm_moe_down(qmm_handle h, qmm_dtype t, const void *const *w_ptrs, const flo
                  size_t workspace_bytes, void *stream) {
     if (!valid_handle(h) || !known_dtype(t) || !w_ptrs || !scales || !hact || !y) return QMM_ERR_INVALID_ARG;
     if (n_used < 1 || t_tokens < 1 || static_cast<int64_t>(n_used) * t_tokens > 4096) return QMM_ERR_SHAPE;
-    if (gin < 1 || gin > kMaxMN || n_ff < 1 || n_ff > kMaxK || qmm_row_bytes(t, n_ff) == 0) return QMM_ERR_SHAPE;
+    if (gin < 1 || gin > kMaxMN || n_ff < 1 || n_ff > kMaxK || !k_ok(t, n_ff)) return QMM_ERR_SHAPE;
     if ((reinterpret_cast<uintptr_t>(w_ptrs) & 7u) != 0 || (reinterpret_cast<uintptr_t>(scales) & 3u) != 0 ||
         !aligned16(hact) || !aligned16(y))
         return QMM_ERR_ALIGN;
@@ -261,13 +270,25 @@ int qmm_moe_down(qmm_handle h, qmm_dtype t, const void *const *w_ptrs, const flo
 int qmm_dequant(qmm_handle h, qmm_dtype t, const void *w, float *out, int64_t m, int64_t k, float tensor_scale,
                 void *stream) {
     if (!valid_handle(h) || !known_dtype(t) || !w || !out) return QMM_ERR_INVALID_ARG;
-    if (m < 1 || m > kMaxMN || k < 1 || k > kMaxK || qmm_row_bytes(t, k) == 0) return QMM_ERR_SHAPE;
+    if (m < 1 || m > kMaxMN || k < 1 || k > kMaxK || !k_ok(t, k)) return QMM_ERR_SHAPE;
     if (!aligned16(w) || !aligned16(out)) return QMM_ERR_ALIGN;
     if (overlaps(out, static_cast<size_t>(m * k) * sizeof(float), w, static_cast<size_t>(qmm_row_bytes(t, k) * m)))
         return QMM_ERR_OVERLAP;
     const int64_t rb = qmm_row_bytes(t, k);
     return on_device(h, [&] {
         return qmm::launch_dequant(t, w, out, m, k, rb, tensor_scale, h->num_sms, static_cast<cudaStream_t>(stream));
+    });
+}
+
+int qmm_nvfp4_repack_v2(qmm_handle h, const void *v1, void *v2, int64_t m, int64_t k, void *stream) {
+    if (!valid_handle(h) || !v1 || !v2) return QMM_ERR_INVALID_ARG;
+    if (m < 1 || m > kMaxMN || k < 64 || k > kMaxK || k % 64 != 0) return QMM_ERR_SHAPE;
+    if (!aligned16(v1) || !aligned16(v2)) return QMM_ERR_ALIGN;
+    const size_t bytes = static_cast<size_t>(qmm_row_bytes(QMM_NVFP4, k) * m);
+    if (overlaps(v1, bytes, v2, bytes)) return QMM_ERR_OVERLAP;
+    return on_device(h, [&] {
+        return qmm::launch_nvfp4_repack_v2(static_cast<const uint8_t *>(v1), static_cast<uint8_t *>(v2), m, k,
+                                           h->num_sms, static_cast<cudaStream_t>(stream));
     });
 }
 

@@ -3,7 +3,8 @@
 // module doc).
 //
 // One thread decodes 8 consecutive weights and writes them as two 16-byte
-// stores; the grid strides over the m*k/8 groups.  Bit-exact: every value is
+// stores; the grid strides over the m*k/8 groups.  The file also holds the
+// repack of NVFP4 rows into the V2 layout (a byte permutation).  Bit-exact: every value is
 // the format's value rounded once to float32 (decode.cuh).
 #include "kernels.h"
 #include "decode.cuh"
@@ -55,6 +56,70 @@ __global__ void __launch_bounds__(256) copy_f32_kernel(const float *__restrict__
         out[i] = __ldg(w + i);
 }
 
+// NVFP4 V2 rows (k/2 code bytes, then k/16 E4M3 scale bytes; k % 64 == 0,
+// so every row starts on a 4-byte boundary): one thread decodes 8
+// consecutive weights from one code word and one scale byte, each value
+// (e2m1 * e4m3, exact) times ts rounded once, as for the 36-byte groups.
+__global__ void __launch_bounds__(256) dequant_nvfp4_v2_kernel(const uint8_t *__restrict__ w,
+                                                               float *__restrict__ out, int64_t m, int64_t k,
+                                                               float ts) {
+    const int64_t rb = k / 32 * 18;
+    if (threadIdx.x == 0) {
+        const uint64_t wb = static_cast<uint64_t>(m) * static_cast<uint64_t>(rb);
+        const uint64_t chunk = (wb + gridDim.x - 1) / gridDim.x;
+        const uint64_t b0 = static_cast<uint64_t>(blockIdx.x) * chunk;
+        const uint64_t b1 = b0 + chunk < wb ? b0 + chunk : wb;
+        if (b0 < b1)
+            prefetch_l2_range(reinterpret_cast<uintptr_t>(w) + b0, reinterpret_cast<uintptr_t>(w) + b1);
+    }
+    griddep_wait();
+    griddep_launch();
+    const int64_t gpr = k / 8;
+    const int64_t total = m * gpr;
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < total;
+         g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = g / gpr;
+        const int64_t e0 = (g - r * gpr) * 8;
+        const uint8_t *row = w + r * rb;
+        const uint32_t codes = __ldg(reinterpret_cast<const unsigned int *>(row + e0 / 2));
+        const float s = e4m3_to_f32(__ldg(row + k / 2 + e0 / 16));
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(__fmul_rn(e2m1_to_f32((codes >> (4 * j)) & 15u), s), ts);
+        float4 *o = reinterpret_cast<float4 *>(out + r * k + e0);
+        o[0] = make_float4(v[0], v[1], v[2], v[3]);
+        o[1] = make_float4(v[4], v[5], v[6], v[7]);
+    }
+}
+
+// NVFP4 36-byte groups -> V2 rows: one thread moves one group (nine 4-byte
+// words; rows of k/64*36 bytes keep every group 4-byte aligned), its 32 code
+// bytes to 32g of the row and its 4 scale bytes to k/2 + 4g.
+__global__ void __launch_bounds__(256) nvfp4_repack_v2_kernel(const uint8_t *__restrict__ v1,
+                                                              uint8_t *__restrict__ v2, int64_t m, int64_t k) {
+    griddep_wait();
+    griddep_launch();
+    const int64_t gpr = k / 64, rb = gpr * 36, total = m * gpr;
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < total;
+         g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = g / gpr, q = g - r * gpr;
+        const unsigned int *src = reinterpret_cast<const unsigned int *>(v1 + r * rb + q * 36);
+        unsigned int *codes = reinterpret_cast<unsigned int *>(v2 + r * rb + q * 32);
+        unsigned int *scales = reinterpret_cast<unsigned int *>(v2 + r * rb + k / 2 + q * 4);
+        *scales = __ldg(src);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) codes[j] = __ldg(src + 1 + j);
+    }
+}
+
+cudaError_t launch_nvfp4_repack_v2(const uint8_t *v1, uint8_t *v2, int64_t m, int64_t k, int num_sms,
+                                   cudaStream_t st) {
+    const int64_t total = m * (k / 64);
+    const int64_t want = (total + 255) / 256;
+    const int grid = static_cast<int>(want < 8LL * num_sms ? want : 8LL * num_sms);
+    return launch_pdl(nvfp4_repack_v2_kernel, dim3(grid), dim3(256), 0, st, dim3(1, 1, 1), v1, v2, m, k);
+}
+
 template <int F>
 static cudaError_t launch_dequant_t(const void *w, float *out, int64_t m, int64_t k, int64_t rb, float ts,
                                     int num_sms, cudaStream_t st) {
@@ -82,6 +147,12 @@ cudaError_t launch_dequant(int dtype, const void *w, float *out, int64_t m, int6
     case QMM_Q4_K: return launch_dequant_t<QMM_Q4_K>(w, out, m, k, rb, ts, num_sms, st);
     case QMM_Q6_K: return launch_dequant_t<QMM_Q6_K>(w, out, m, k, rb, ts, num_sms, st);
     case QMM_NVFP4: return launch_dequant_t<QMM_NVFP4>(w, out, m, k, rb, ts, num_sms, st);
+    case QMM_NVFP4_V2: {
+        const int64_t want = (m * (k / 8) + 255) / 256;
+        const int grid = static_cast<int>(want < 8LL * num_sms ? want : 8LL * num_sms);
+        return launch_pdl(dequant_nvfp4_v2_kernel, dim3(grid), dim3(256), 0, st, dim3(1, 1, 1),
+                          static_cast<const uint8_t *>(w), out, m, k, ts);
+    }
     default: return cudaErrorInvalidValue;
     }
 }

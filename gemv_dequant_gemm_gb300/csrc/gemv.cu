@@ -238,6 +238,21 @@ template <> __device__ __forceinline__ void grp8<QMM_NVFP4>(const uint8_t *row, 
     }
 }
 
+// NVFP4 V2 row (k/2 code bytes, then k/16 E4M3 scale bytes): the same
+// decode as the 36-byte groups, with the codes at e0/2 and the scale at
+// k/2 + e0/16 (k % 64 == 0 keeps the code word 4-byte aligned).
+template <> __device__ __forceinline__ void grp8<QMM_NVFP4_V2>(const uint8_t *row, int64_t e0, int64_t k, Grp &g) {
+    g.scale = 0.5f * e4m3_to_f32(LdS::u8(row + (k >> 1) + (e0 >> 4)));  // the bytes below hold 2 * value
+    g.offset = 0.0f;
+    const uint32_t codes = LdS::u32(row + (e0 >> 1));
+    const uint32_t lo = e2m1x4_offset_bytes(codes & 0xFFFFu), hi = e2m1x4_offset_bytes(codes >> 16);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        g.v[j] = byte_as_float(lo, j, 8388620.0f);  // (2v + 12) - 12
+        g.v[4 + j] = byte_as_float(hi, j, 8388620.0f);
+    }
+}
+
 // 8 consecutive X values of one activation row (shared or global memory).
 __device__ __forceinline__ void load_x8(const float *xr, bool in_smem, int64_t e0, int64_t k, float (&v)[8]) {
     if (e0 + 8 <= k && (k % 4) == 0) {
@@ -523,7 +538,8 @@ struct Ctl {
     int pad;
 };
 
-template <int F> struct Unit { static constexpr int W = (F == QMM_NVFP4) ? 16 : 8; };
+template <int F> constexpr bool is_fp4() { return F == QMM_NVFP4 || F == QMM_NVFP4_V2; }
+template <int F> struct Unit { static constexpr int W = is_fp4<F>() ? 16 : 8; };
 template <int NV> constexpr int nv_pow2() { return NV <= 1 ? 1 : (NV <= 2 ? 2 : (NV <= 4 ? 4 : 8)); }
 template <int F, int NV> constexpr int jmax() {
     return XREG / (NV * Unit<F>::W) >= 1 ? XREG / (NV * Unit<F>::W) : 1;
@@ -803,6 +819,13 @@ __global__ void __launch_bounds__(gr::THREADS, 1) gemv_rx_kernel(const gr::Param
                 scoff[jj] = blk + (e >> 4);
                 cdoff[jj] = blk + 4u + (e >> 1);
             }
+        } else if constexpr (F == QMM_NVFP4_V2) {
+#pragma unroll
+            for (int jj = 0; jj < JM; ++jj) {
+                const uint32_t e0 = static_cast<uint32_t>(tk + p.tk * jj) * 16u;
+                scoff[jj] = static_cast<uint32_t>(p.k >> 1) + (e0 >> 4);
+                cdoff[jj] = e0 >> 1;
+            }
         }
         int cur_tok = -1;
         bool dead = false;
@@ -824,7 +847,7 @@ __global__ void __launch_bounds__(gr::THREADS, 1) gemv_rx_kernel(const gr::Param
 #pragma unroll
                         for (int w = 0; w < UW; ++w) t += xr[jj][v][w];
                         xs[jj][v] = t;
-                        if constexpr (F == QMM_NVFP4) {
+                        if constexpr (is_fp4<F>()) {
 #pragma unroll
                             for (int q = 0; q < 8; ++q)
                                 x2[jj][v][q] = f2_pack(xr[jj][v][2 * q], xr[jj][v][2 * q + 1]);
@@ -858,7 +881,7 @@ __global__ void __launch_bounds__(gr::THREADS, 1) gemv_rx_kernel(const gr::Param
 #pragma unroll
                         for (int jj = 0; jj < JM; ++jj) {
                             const int u = tk + p.tk * jj;
-                            if constexpr (F == QMM_NVFP4) {
+                            if constexpr (is_fp4<F>()) {
                                 uint64_t w2[8];
                                 float sc;
                                 nvfp4_unit16(rbase + cdoff[jj], rbase + scoff[jj], w2, sc);
@@ -1037,6 +1060,7 @@ static cudaError_t dispatch_any(int dtype, const gr::Params &rp, const gv::Param
     case QMM_Q4_K: return launch_any_f<QMM_Q4_K>(rp, gp, n, num_sms, st);
     case QMM_Q6_K: return launch_any_f<QMM_Q6_K>(rp, gp, n, num_sms, st);
     case QMM_NVFP4: return launch_any_f<QMM_NVFP4>(rp, gp, n, num_sms, st);
+    case QMM_NVFP4_V2: return launch_any_f<QMM_NVFP4_V2>(rp, gp, n, num_sms, st);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -30,6 +30,10 @@ cudaError_t launch_moe_down(int dtype, const void *const *w_ptrs, int64_t rb, co
                             float *y, float *part, int64_t n_ff, int64_t gin, int n_used, int tokens, int num_sms,
                             uint32_t *status, uint64_t limit_ns, cudaStream_t st);
 
+// NVFP4 36-byte-group rows -> V2 rows (codes, then the scale stream); k % 64 == 0.
+cudaError_t launch_nvfp4_repack_v2(const uint8_t *v1, uint8_t *v2, int64_t m, int64_t k, int num_sms,
+                                   cudaStream_t st);
+
 // Tensor-core GEMM for n > QMM_GEMV_MAX_N.  x16 is the f16 workspace (packed
 // formats only).  status: the handle's device status word.
 struct GemmArgs {

@@ -66,16 +66,17 @@ bool overlaps(const void *a, size_t abytes, const void *b, size_t bbytes) {
 
 extern "C" int qmm_gemm_noalloc(qmm_dtype t, const void *w, const float *x, float *dst, int64_t m, int64_t k,
                                 int64_t n, void *stream) {
-    if (!w || !x || !dst || t < QMM_F32 || t > QMM_NVFP4) return QMM_ERR_INVALID_ARG;
+    if (!w || !x || !dst || t < QMM_F32 || t > QMM_NVFP4_V2) return QMM_ERR_INVALID_ARG;
     if (m < 1 || n < 1 || m > kMaxMN || n > kMaxMN || k < 1 || k > kMaxK) return QMM_ERR_SHAPE;
     const int64_t rb = qmm_row_bytes(t, k);
-    if (rb == 0) return QMM_ERR_SHAPE;
+    if (rb == 0 || (t == QMM_NVFP4_V2 && k % 64 != 0)) return QMM_ERR_SHAPE;
     if (!aligned16(w) || !aligned16(x) || !aligned16(dst)) return QMM_ERR_ALIGN;
     const size_t dbytes = static_cast<size_t>(n * m) * sizeof(float);
     if (overlaps(dst, dbytes, w, static_cast<size_t>(rb * m)) ||
         overlaps(dst, dbytes, x, static_cast<size_t>(n * k) * sizeof(float)))
         return QMM_ERR_OVERLAP;
     const bool tensor_core = n > QMM_GEMV_MAX_N;
+    if (tensor_core && t == QMM_NVFP4_V2) return QMM_ERR_UNSUPPORTED;  // the tensor-core decode reads 36-byte groups
     if (tensor_core && t == QMM_F32 && k % 4 != 0) return QMM_ERR_SHAPE;
     const size_t need = tensor_core ? qmm_gemm_workspace_bytes(t, m, k, n) : 0;
     if (need > kScratch - kStatusBytes) return QMM_ERR_WORKSPACE;

@@ -32,6 +32,17 @@
  *   QMM_NVFP4  64 / 36   4 E4M3 scale bytes (one per 16 weights), 32 bytes of
  *                        E2M1 codes, low nibble of byte j = element 2j;
  *                        value e2m1*e4m3
+ *   QMM_NVFP4_V2 32 / 18 the same values with the scales split out: a row is
+ *                        its k/2 code bytes (low nibble of byte j = element
+ *                        2j), then its k/16 E4M3 scale bytes (byte s covers
+ *                        elements 16s..16s+15); 18 bytes per 32 weights as in
+ *                        the V2 arms of memra-engine 0.128.0
+ *                        moe_rows_ceiling_bench.rs (main), built from
+ *                        QMM_NVFP4 rows by qmm_nvfp4_repack_v2.  The calls
+ *                        take it with k % 64 == 0 (aligned code words), in
+ *                        qmm_gemv, qmm_moe_gemv, qmm_moe_down and qmm_dequant;
+ *                        qmm_gemm and qmm_gemm_noalloc with n > QMM_GEMV_MAX_N
+ *                        return QMM_ERR_UNSUPPORTED for it.
  * The bit orders inside Q4_K and Q6_K are the ggml k-quant orders.
  *
  * Conventions shared by every call:
@@ -73,7 +84,8 @@ typedef enum {
     QMM_Q8_0 = 2,
     QMM_Q4_K = 3,
     QMM_Q6_K = 4,
-    QMM_NVFP4 = 5
+    QMM_NVFP4 = 5,
+    QMM_NVFP4_V2 = 6
 } qmm_dtype;
 
 /* Status codes. */
@@ -196,6 +208,18 @@ size_t qmm_moe_down_workspace_bytes(int64_t gin, int n_used, int t_tokens);
 int qmm_moe_down(qmm_handle h, qmm_dtype t, const void *const *w_ptrs, const float *scales,
                  const float *hact, float *y, int64_t n_ff, int64_t gin, int n_used, int t_tokens,
                  void *workspace, size_t workspace_bytes, void *stream);
+
+/* Repack NVFP4 rows into the V2 layout (memra-engine 0.128.0
+ * src/bin/moe_rows_ceiling_bench.rs, main: the V2 arms read the same values
+ * through rows repacked with the scales split out).  v1 is [m] rows of
+ * k/64 * 36 bytes (QMM_NVFP4), v2 receives [m] rows of k/32 * 18 bytes
+ * (QMM_NVFP4_V2): for every row, 64-weight group g's 32 code bytes go to
+ * bytes 32g..32g+31 of the row and its 4 scale bytes to bytes k/2 + 4g ..
+ * k/2 + 4g + 3.  A pure byte permutation: every weight keeps its value.
+ * Device pointers, both 16-byte aligned and not overlapping; 1 <= m <= 2^24,
+ * 64 <= k <= 2^20, k % 64 == 0.  Errors: QMM_ERR_INVALID_ARG, QMM_ERR_SHAPE,
+ * QMM_ERR_ALIGN, QMM_ERR_OVERLAP, QMM_ERR_CUDA. */
+int qmm_nvfp4_repack_v2(qmm_handle h, const void *v1, void *v2, int64_t m, int64_t k, void *stream);
 
 /* Standalone dequant (aprender-serve cublas_prefill/mod.rs module doc, v1
  * path, which dequantizes Q4K/Q6K weights into an FP32 scratch buffer):

@@ -32,7 +32,7 @@ def test_every_declared_symbol_is_exported():
 
 
 def test_row_bytes_agree_with_the_oracle():
-    for fmt in ("f32", "q4_0", "q8_0", "q4_k", "q6_k", "nvfp4"):
+    for fmt in ("f32", "q4_0", "q8_0", "q4_k", "q6_k", "nvfp4", "nvfp4_v2"):
         assert q.qmm_block_weights(fmt) == oracle.block_weights(fmt)
         assert q.qmm_block_bytes(fmt) == oracle.block_bytes(fmt)
         for k in (1, 32, 64, 96, 256, 1000, 1024, 4096, 4608):
@@ -47,6 +47,7 @@ def test_workspace_bytes():
     assert q.qmm_gemm_workspace_bytes("q4_0", 64, 32, 9) == 768  # 576 rounded up to 256
     assert q.qmm_gemm_workspace_bytes("q8_0", 64, 64, 8) == 0    # GEMV regime
     assert q.qmm_gemm_workspace_bytes("f32", 64, 64, 512) == 0   # tf32 path reads X directly
+    assert q.qmm_gemm_workspace_bytes("nvfp4_v2", 64, 64, 512) == 0  # no tensor-core path for V2
     assert q.qmm_moe_down_workspace_bytes(4096, 8, 1) == 8 * 4096 * 4
     assert q.qmm_moe_down_workspace_bytes(101, 3, 2) == 2560     # 2424 rounded up to 256
     assert q.qmm_moe_down_workspace_bytes(4096, 1, 5) == 0       # one expert: products go straight to y
@@ -67,6 +68,8 @@ def test_null_handle_and_arguments_are_rejected_without_a_device():
     assert lib.qmm_dequant(None, 1, 16, 16, 32, 32, 1.0, None) == 1
     assert lib.qmm_moe_gemv(None, 5, 16, 16, 16, 16, 64, 16, 1, 1, None) == 1
     assert lib.qmm_moe_down(None, 5, 16, 16, 16, 16, 64, 16, 2, 1, 16, 256, None) == 1
+    assert lib.qmm_nvfp4_repack_v2(None, 16, 16, 1, 64, None) == 1
+    assert lib.qmm_gemm_noalloc(7, 16, 16, 16, 16, 64, 16, None) == 1  # unknown dtype
     assert lib.qmm_sync_status(None, None) == 1
     assert lib.qmm_destroy(None) == 0
     assert lib.qmm_create(0, None) == 1

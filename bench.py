@@ -422,9 +422,43 @@ def _time_calls(torch, stream, calls, reps):
     return e0.elapsed_time(e1) / reps
 
 
+def _moe_v2_sub(q, lib, h, torch, stream, keep, scales, x, y, in_f, n_ff, n_used, n_pairs, wbytes, hbm_gbs):
+    sptr = stream.cuda_stream
+    mat_bytes = n_ff * q.qmm_row_bytes("nvfp4", in_f)
+    keep2, tables2 = [], []
+    for c in range(len(keep) // (2 * n_pairs)):
+        ptrs = []
+        for i in range(2 * n_pairs):
+            src = keep[c * 2 * n_pairs + i]
+            dst = torch.empty_like(src)
+            st = lib.qmm_nvfp4_repack_v2(h, src.data_ptr(), dst.data_ptr(), n_ff, in_f, sptr)
+            if st != 0:
+                raise RuntimeError(f"qmm_nvfp4_repack_v2 status {st}")
+            keep2.append(dst)
+            ptrs.append(dst.data_ptr())
+        tables2.append(torch.tensor(ptrs + [0] * n_pairs, dtype=torch.int64, device="cuda"))
+    calls = [(lambda tb=tb: lib.qmm_moe_gemv(h, q.NVFP4_V2, tb.data_ptr(), scales.data_ptr(), x.data_ptr(),
+                                             y.data_ptr(), in_f, n_ff, n_used, 1, sptr)) for tb in tables2]
+    if calls[0]() != 0:
+        raise RuntimeError("qmm_moe_gemv refused the V2 table")
+    ms = _time_calls(torch, stream, calls, 40)
+    gbs = wbytes / (ms * 1e-3) / 1e9
+    moe_v2 = {"us": round(ms * 1e3, 3), "weight_bytes": wbytes, "weight_gbs": round(gbs, 1),
+              "frac_hbm": round(gbs / hbm_gbs, 4)}
+    pairs = list(zip(keep, keep2))
+    calls = [(lambda s=s_, d=d_: lib.qmm_nvfp4_repack_v2(h, s.data_ptr(), d.data_ptr(), n_ff, in_f, sptr))
+             for s_, d_ in pairs]
+    ms = _time_calls(torch, stream, calls, len(calls))
+    gbs = 2 * mat_bytes / (ms * 1e-3) / 1e9
+    repack = {"m": n_ff, "k": in_f, "us": round(ms * 1e3, 3), "bytes": 2 * mat_bytes, "gbs": round(gbs, 1),
+              "frac_hbm": round(gbs / hbm_gbs, 4)}
+    del keep2, tables2
+    return moe_v2, repack
+
+
 def run_sub_benches(q, lib, h, torch, synth, stream, hbm_gbs):
     sptr = stream.cuda_stream
-    out = {"gemv": [], "moe": None, "moe_down": None, "dequant": []}
+    out = {"gemv": [], "moe": None, "moe_v2": None, "repack_v2": None, "moe_down": None, "dequant": []}
     # GEMV: rotate over enough weight copies to exceed L2 several times
     for fmt in ("q4_k", "q8_0"):
         for m, k in ((4608, 1024), (1024, 4608)):
@@ -466,6 +500,13 @@ def run_sub_benches(q, lib, h, torch, synth, stream, hbm_gbs):
     gbs = wbytes / (ms * 1e-3) / 1e9
     out["moe"] = {"us": round(ms * 1e3, 3), "weight_bytes": wbytes, "weight_gbs": round(gbs, 1),
                   "frac_hbm": round(gbs / hbm_gbs, 4)}
+    # the same call on V2 rows (codes, then the scale stream) made by the
+    # library's repack, and the repack itself (read + write of each matrix)
+    try:
+        out["moe_v2"], out["repack_v2"] = _moe_v2_sub(q, lib, h, torch, stream, keep, scales, x, y, in_f, n_ff,
+                                                      n_used, n_pairs, wbytes, hbm_gbs)
+    except Exception as exc:  # reported in the JSON line, never fatal to the headline measurement
+        out["moe_v2"] = {"error": f"{type(exc).__name__}: {exc}"}
     del keep, tables
     # MoE down projection: 8 experts of [gin 4096][n_ff 2048], per-pair
     # activations, pairs summed into y; 6 rotated copies of the weight set

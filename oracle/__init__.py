@@ -78,6 +78,11 @@ def _load():
                                     I64, I64, P, P, ctypes.c_int]
     lib.oracle_nvfp4_repack_v2.restype = ctypes.c_int
     lib.oracle_nvfp4_repack_v2.argtypes = [P, P, I64, I64]
+    lib.oracle_quantize_q8_1.restype = ctypes.c_int
+    lib.oracle_quantize_q8_1.argtypes = [P, I64, I64, P, P]
+    lib.oracle_moe_gate_up_q8.restype = ctypes.c_int
+    lib.oracle_moe_gate_up_q8.argtypes = [ctypes.c_int, P, P, P, P, I64, I64, ctypes.c_int, ctypes.c_int,
+                                          I64, I64, P, P, ctypes.c_int]
     lib.oracle_max_threads.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     _lib = lib
@@ -222,6 +227,44 @@ def moe_gate_up(fmt: str, mats, scales, x, in_f: int, n_ff: int, n_used: int, t:
                                     row0, nrows, _ptr(y), _ptr(am), threads)
     if rc:
         raise ValueError(f"oracle_moe_gate_up failed ({rc})")
+    return y, am
+
+
+def quantize_q8_1(x, rows: int, k: int):
+    """(q int8 [rows][k], d float32 [rows][k/32]): Q8_1 blocks of 32 values,
+    d = amax/127, q = x*(1/d) rounded half away from zero, all in float32."""
+    xa = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+    if xa.size != rows * k:
+        raise ValueError("x has the wrong size")
+    q = np.empty((rows, k), np.int8)
+    d = np.empty((rows, k // 32 if k > 0 else 0), np.float32)
+    rc = _load().oracle_quantize_q8_1(_ptr(xa), rows, k, _ptr(q), _ptr(d))
+    if rc:
+        raise ValueError(f"oracle_quantize_q8_1 failed ({rc})")
+    return q, d
+
+
+def moe_gate_up_q8(fmt: str, mats, scales, q, d, in_f: int, n_ff: int, n_used: int, t: int,
+                   row0: int = 0, nrows: int | None = None, threads: int = 0):
+    """moe_gate_up with each token's activation given as Q8_1 blocks (q, d):
+    x[tok][c] = q[tok][c] * d[tok][c // 32]."""
+    n_pairs = t * n_used
+    if len(mats) != 2 * n_pairs:
+        raise ValueError("need 2*n_pairs matrices")
+    nrows = n_ff if nrows is None else nrows
+    keep = [_wbytes(a) for a in mats]
+    table = np.array([_ptr(a) for a in keep], dtype=np.uint64)
+    sc = np.ascontiguousarray(scales, dtype=np.float32)
+    qa = np.ascontiguousarray(q, dtype=np.int8).reshape(-1)
+    da = np.ascontiguousarray(d, dtype=np.float32).reshape(-1)
+    if qa.size != t * in_f or da.size != t * (in_f // 32):
+        raise ValueError("q or d has the wrong size")
+    y = np.full((2, n_pairs, n_ff), np.nan)
+    am = np.full((2, n_pairs, n_ff), np.nan)
+    rc = _load().oracle_moe_gate_up_q8(_fmt(fmt), _ptr(table), _ptr(sc), _ptr(qa), _ptr(da), in_f, n_ff, n_used,
+                                       t, row0, nrows, _ptr(y), _ptr(am), threads)
+    if rc:
+        raise ValueError(f"oracle_moe_gate_up_q8 failed ({rc})")
     return y, am
 
 

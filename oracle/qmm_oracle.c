@@ -467,6 +467,77 @@ int oracle_moe_gate_up(int fmt, const uint8_t *const *mats, const float *scales,
 }
 
 /* ---------------------------------------------------------------------- */
+/* int8 activations ([memra] main: quantize_q8_1 before the served gate/up   */
+/* kernel; the page prints neither, so the block rule is the plain Q8_1     */
+/* one: 32 values per block, one scale per block)                           */
+/* ---------------------------------------------------------------------- */
+
+/* For every block of 32 consecutive values of a row of x ([rows][k], k a
+ * multiple of 32): amax = the largest |x|, d = amax / 127, and every value
+ * becomes q = x * (1/d) rounded to the nearest integer, halves away from
+ * zero (q = 0 when d = 0).  Every step is one float32 operation, so the
+ * integer codes are decided in float32.  d is [rows][k/32], q [rows][k]. */
+int oracle_quantize_q8_1(const float *x, int64_t rows, int64_t k, int8_t *q, float *d) {
+    if (rows < 0 || k <= 0 || k % 32 != 0) return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b = 0; b < k / 32; ++b) {
+            const float *xb = x + r * k + 32 * b;
+            float amax = 0.0f;
+            for (int j = 0; j < 32; ++j) {
+                float a = fabsf(xb[j]);
+                if (a > amax) amax = a;
+            }
+            float db = amax / 127.0f;
+            float id = db != 0.0f ? 1.0f / db : 0.0f;
+            d[r * (k / 32) + b] = db;
+            for (int j = 0; j < 32; ++j) q[r * k + 32 * b + j] = (int8_t)roundf(xb[j] * id);
+        }
+    }
+    return 0;
+}
+
+/* The gate/up products of oracle_moe_gate_up with each token's activation
+ * given as Q8_1 blocks: x[tok][c] = q[tok][c] * d[tok][c/32], exact in
+ * double, the rest unchanged. */
+int oracle_moe_gate_up_q8(int fmt, const uint8_t *const *mats, const float *scales, const int8_t *q,
+                          const float *d, int64_t in_f, int64_t n_ff, int n_used, int t, int64_t row0,
+                          int64_t nrows, double *y, double *absmag, int threads) {
+    int64_t rb = oracle_row_bytes(fmt, in_f);
+    if (rb == 0 || in_f % 32 != 0 || n_used <= 0 || t <= 0) return -1;
+    int64_t n_pairs = (int64_t)t * n_used;
+    if (row0 < 0 || nrows < 0 || row0 + nrows > n_ff) return -1;
+    int bad = 0;
+#ifdef _OPENMP
+    if (threads > 0) omp_set_num_threads(threads);
+#pragma omp parallel for schedule(dynamic, 16) reduction(| : bad)
+#endif
+    for (int64_t idx = 0; idx < 2 * n_pairs * nrows; ++idx) {
+        int64_t mat = idx / nrows;
+        int64_t r = row0 + idx % nrows;
+        int64_t tok = (mat % n_pairs) / n_used;
+        double *row = (double *)malloc(sizeof(double) * (size_t)in_f);
+        if (!row || oracle_decode_row(fmt, mats[mat] + r * rb, in_f, row) != 0) {
+            bad |= 1;
+            free(row);
+            continue;
+        }
+        double s = 0.0, a = 0.0;
+        for (int64_t c = 0; c < in_f; ++c) {
+            double xv = (double)q[tok * in_f + c] * (double)d[tok * (in_f / 32) + c / 32];
+            double p = row[c] * xv;
+            s += p;
+            a += fabs(p);
+        }
+        double sc = (double)scales[mat];
+        y[mat * n_ff + r] = sc * s;
+        if (absmag) absmag[mat * n_ff + r] = fabs(sc) * a;
+        free(row);
+    }
+    (void)threads;
+    return bad ? -1 : 0;
+}
+
+/* ---------------------------------------------------------------------- */
 /* MoE down projection ([memra] main: the down pass after gate/up)        */
 /* ---------------------------------------------------------------------- */
 

@@ -438,3 +438,77 @@ def test_nvfp4_repack_v2_is_the_split_of_the_groups():
     assert np.array_equal(a, b) and np.array_equal(am, bm)
     with pytest.raises(ValueError):
         oracle.nvfp4_repack_v2(v1[:36], 1, 32)  # k must be a multiple of 64
+
+
+# ---- Q8_1 activation blocks (int8 codes, one float32 scale per 32 values) ----
+
+
+def test_q8_1_hand_block():
+    # amax 127 gives d = 1, so every code is its value rounded, halves away from zero
+    x = np.zeros((1, 64), np.float32)
+    x[0, :8] = [127.0, -63.5, 0.5, -0.5, 1.49, -2.5, 126.6, 0.0]
+    q, d = oracle.quantize_q8_1(x, 1, 64)
+    assert q[0, :8].tolist() == [127, -64, 1, -1, 1, -3, 127, 0]
+    assert np.all(q[0, 8:] == 0)
+    assert d.tolist() == [[1.0, 0.0]]  # the all-zero second block has scale 0
+
+
+def test_q8_1_block_boundaries_and_scales():
+    # block 0 peaks at 127/8 (d = 1/8), block 1 at 127*4 (d = 4): both exact
+    # in binary, so x/d is exact and only the half-away rounding acts; index 40
+    # lies in block 1
+    x = np.zeros((1, 64), np.float32)
+    x[0, 3] = 127 / 8
+    x[0, 5] = 0.0625      # x/d = 0.5  -> 1
+    x[0, 6] = -0.1875     # x/d = -1.5 -> -2
+    x[0, 40] = -127 * 4
+    x[0, 41] = 6.0        # x/d = 1.5  -> 2
+    x[0, 42] = -10.0      # x/d = -2.5 -> -3
+    q, d = oracle.quantize_q8_1(x, 1, 64)
+    assert d.tolist() == [[0.125, 4.0]]
+    assert (q[0, 3], q[0, 5], q[0, 6]) == (127, 1, -2)
+    assert (q[0, 40], q[0, 41], q[0, 42]) == (-127, 2, -3)
+
+
+def test_q8_1_invariants_on_random_rows():
+    import synth
+    rows, k = 4, 4096
+    x = synth.activations(rows, k)
+    q, d = oracle.quantize_q8_1(x, rows, k)
+    xb = x.reshape(rows, k // 32, 32).astype(np.float64)
+    qb = q.reshape(rows, k // 32, 32).astype(np.float64)
+    db = d.astype(np.float64)[:, :, None]
+    assert np.all(np.abs(qb) <= 127)
+    assert np.all(np.abs(qb).max(axis=2) == 127)  # the block's largest value maps to +-127
+    assert np.all(np.abs(xb - qb * db) <= 0.5 * db * (1 + 1e-6))
+
+
+def test_moe_gate_up_q8_equals_the_float_path_on_exact_activations():
+    import synth
+    # integer activations with +-127 in every block: d = 1 and q = x, so the
+    # Q8_1 product must equal the pinned float product exactly
+    in_f, n_ff, n_used, t = 128, 16, 2, 2
+    n_pairs = n_used * t
+    rng = np.random.default_rng(5)
+    x = rng.integers(-127, 128, (t, in_f)).astype(np.float32)
+    x[:, ::32] = 127.0
+    mats = [synth.nvfp4_rows(synth.nvfp4_matrix_seed(3, j, p), n_ff, in_f) for p in range(2) for j in range(n_pairs)]
+    scales = np.array([0.5 + 0.01 * p for p in range(2 * n_pairs)], np.float32)
+    q, d = oracle.quantize_q8_1(x, t, in_f)
+    assert np.all(d == 1.0) and np.array_equal(q.astype(np.float32), x)
+    y8, a8 = oracle.moe_gate_up_q8("nvfp4", mats, scales, q, d, in_f, n_ff, n_used, t)
+    yf, af = oracle.moe_gate_up("nvfp4", mats, scales, x, in_f, n_ff, n_used, t)
+    assert np.array_equal(y8, yf) and np.array_equal(a8, af)
+
+
+def test_moe_gate_up_q8_all_ones_weights():
+    # W all ones: y = scale * sum_c q[c] * d[c // 32]
+    in_f, n_ff, n_used, t = 128, 4, 1, 1
+    grp = bytes([0x38] * 4 + [0x22] * 32)
+    mat = np.frombuffer(grp * (n_ff * in_f // 64), np.uint8)
+    x = ((np.arange(in_f, dtype=np.float32) - 50) / 7).reshape(1, in_f)
+    q, d = oracle.quantize_q8_1(x, 1, in_f)
+    scales = np.array([0.75, -1.5], np.float32)
+    y, _ = oracle.moe_gate_up_q8("nvfp4", [mat, mat], scales, q, d, in_f, n_ff, n_used, t)
+    s = sum(float(q[0, c]) * float(d[0, c // 32]) for c in range(in_f))
+    assert np.allclose(y[0, 0], 0.75 * s, rtol=1e-15, atol=0) and np.allclose(y[1, 0], -1.5 * s, rtol=1e-15, atol=0)

@@ -81,6 +81,23 @@ def _dist():
     return world, rank, local
 
 
+def slowest_rank_ms(ms: float, world: int, device: str) -> float:
+    """The largest of the ranks' times (the job ends when its slowest rank
+    does); a collective, so every rank calls it."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, flops_per_rank_step: float, ms_per_step: float) -> float:
+    """Whole-job throughput: the work of every rank over the slowest rank's step time."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 # --------------------------------------------------------------------------
 # clocks
 # --------------------------------------------------------------------------
@@ -307,13 +324,8 @@ def run_ours(args):
         step(s % copies_n, ev_launch[s])
     torch.cuda.synchronize()
     launch_ms = np.array([[a.elapsed_time(b) for a, b in row] for row in ev_launch])  # [steps][gemm]
-    ms_per_step = float(np.mean(step_ms))
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_per_step], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_per_step = float(t.item())
-    value = world * flops_step / (ms_per_step * 1e-3) / 1e12
+    ms_per_step = slowest_rank_ms(float(np.mean(step_ms)), world, "cuda")
+    value = job_tflops(world, flops_step, ms_per_step)
 
     per_gemm = []
     for i, g in enumerate(gemms):
@@ -364,8 +376,8 @@ def run_ours(args):
                     p["dst"].copy_(b["dst"], non_blocking=True)
             ev1.record(stream)
             torch.cuda.synchronize()
-        e2e_ms = ev0.elapsed_time(ev1) / e2e_steps
-        e2e = {"value": round(world * flops_step / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+        e2e_ms = slowest_rank_ms(ev0.elapsed_time(ev1) / e2e_steps, world, "cuda")
+        e2e = {"value": round(job_tflops(world, flops_step, e2e_ms), 3), "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 4)}
 
     # ---- a6-a8: GEMV, MoE, dequant (weight-stream GB/s vs HBM) ----

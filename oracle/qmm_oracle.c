@@ -35,8 +35,9 @@
  *              standalone dequant step)
  *
  * Readings where the pages are silent (the byte orderings inside Q4_K and
- * Q6_K, the NVFP4 nibble order, the MoE output layout) follow the workload
- * definitions stated alongside the benchmark and are listed in the design doc.
+ * Q6_K, the NVFP4 nibble order, the MoE output layout, the V2 row layout, the
+ * Q8_1 block rule) follow the workload definitions stated alongside the
+ * benchmark; each is stated at the function that takes it.
  */
 #include <math.h>
 #include <stdint.h>

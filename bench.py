@@ -557,6 +557,19 @@ def run_sub_benches(q, lib, h, torch, synth, stream, hbm_gbs):
         gbs = tot / (ms * 1e-3) / 1e9
         out["dequant"].append({"dtype": fmt, "m": m, "k": k, "us": round(ms * 1e3, 3), "gbs": round(gbs, 1),
                                "frac_hbm": round(gbs / hbm_gbs, 4)})
+        if fmt == "nvfp4":  # the same rows as V2 (codes, then the scale stream), made by the library's repack
+            try:
+                w2 = torch.empty_like(w)
+                if lib.qmm_nvfp4_repack_v2(h, w.data_ptr(), w2.data_ptr(), m, k, sptr) != 0:
+                    raise RuntimeError("qmm_nvfp4_repack_v2 refused the call")
+                calls = [(lambda o=o: lib.qmm_dequant(h, q.NVFP4_V2, w2.data_ptr(), o.data_ptr(), m, k,
+                                                      1.0, sptr)) for o in outs]
+                ms = _time_calls(torch, stream, calls, 32)
+                gbs = tot / (ms * 1e-3) / 1e9
+                out["dequant"].append({"dtype": "nvfp4_v2", "m": m, "k": k, "us": round(ms * 1e3, 3),
+                                       "gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm_gbs, 4)})
+            except Exception as exc:
+                out["dequant"].append({"dtype": "nvfp4_v2", "error": f"{type(exc).__name__}: {exc}"})
     st = q.qmm_sync_status(h)
     if st != 0:
         raise RuntimeError(f"device status {st} in the sub-benchmarks")

@@ -83,6 +83,9 @@ def _load():
     lib.oracle_moe_gate_up_q8.restype = ctypes.c_int
     lib.oracle_moe_gate_up_q8.argtypes = [ctypes.c_int, P, P, P, P, I64, I64, ctypes.c_int, ctypes.c_int,
                                           I64, I64, P, P, ctypes.c_int]
+    lib.oracle_moe_down_q8.restype = ctypes.c_int
+    lib.oracle_moe_down_q8.argtypes = [ctypes.c_int, P, P, P, P, I64, I64, ctypes.c_int, ctypes.c_int,
+                                       I64, I64, P, P, ctypes.c_int]
     lib.oracle_max_threads.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     _lib = lib
@@ -288,4 +291,28 @@ def moe_down(fmt: str, mats, scales, h, n_ff: int, gin: int, n_used: int, t: int
                                  row0, nrows, _ptr(y), _ptr(am), threads)
     if rc:
         raise ValueError(f"oracle_moe_down failed ({rc})")
+    return y, am
+
+
+def moe_down_q8(fmt: str, mats, scales, q, d, n_ff: int, gin: int, n_used: int, t: int,
+                row0: int = 0, nrows: int | None = None, threads: int = 0):
+    """moe_down with each pair's activation given as Q8_1 blocks (q, d):
+    h[j][c] = q[j][c] * d[j][c // 32]."""
+    n_pairs = t * n_used
+    if len(mats) != n_pairs:
+        raise ValueError("need t*n_used matrices")
+    nrows = gin if nrows is None else nrows
+    keep = [_wbytes(a) for a in mats]
+    table = np.array([_ptr(a) for a in keep], dtype=np.uint64)
+    sc = np.ascontiguousarray(scales, dtype=np.float32)
+    qa = np.ascontiguousarray(q, dtype=np.int8).reshape(-1)
+    da = np.ascontiguousarray(d, dtype=np.float32).reshape(-1)
+    if qa.size != n_pairs * n_ff or da.size != n_pairs * (n_ff // 32):
+        raise ValueError("q or d has the wrong size")
+    y = np.full((t, gin), np.nan)
+    am = np.full((t, gin), np.nan)
+    rc = _load().oracle_moe_down_q8(_fmt(fmt), _ptr(table), _ptr(sc), _ptr(qa), _ptr(da), n_ff, gin, n_used, t,
+                                    row0, nrows, _ptr(y), _ptr(am), threads)
+    if rc:
+        raise ValueError(f"oracle_moe_down_q8 failed ({rc})")
     return y, am

@@ -593,6 +593,53 @@ int oracle_moe_down(int fmt, const uint8_t *const *mats, const float *scales, co
     return bad ? -1 : 0;
 }
 
+/* The down projection of oracle_moe_down with each pair's activation given
+ * as Q8_1 blocks: h[j][c] = q[j][c] * d[j][c/32], exact in double. */
+int oracle_moe_down_q8(int fmt, const uint8_t *const *mats, const float *scales, const int8_t *q,
+                       const float *dsc, int64_t n_ff, int64_t gin, int n_used, int t, int64_t row0,
+                       int64_t nrows, double *y, double *absmag, int threads) {
+    int64_t rb = oracle_row_bytes(fmt, n_ff);
+    if (rb == 0 || n_ff % 32 != 0 || n_used <= 0 || t <= 0) return -1;
+    if (row0 < 0 || nrows < 0 || row0 + nrows > gin) return -1;
+    int bad = 0;
+#ifdef _OPENMP
+    if (threads > 0) omp_set_num_threads(threads);
+#pragma omp parallel for schedule(dynamic, 16) reduction(| : bad)
+#endif
+    for (int64_t idx = 0; idx < (int64_t)t * nrows; ++idx) {
+        int64_t i = idx / nrows;
+        int64_t r = row0 + idx % nrows;
+        double *row = (double *)malloc(sizeof(double) * (size_t)n_ff);
+        if (!row) {
+            bad |= 1;
+            continue;
+        }
+        double s = 0.0, a = 0.0;
+        for (int u = 0; u < n_used; ++u) {
+            int64_t j = i * n_used + u;
+            if (oracle_decode_row(fmt, mats[j] + r * rb, n_ff, row) != 0) {
+                bad |= 1;
+                break;
+            }
+            double dd = 0.0, m = 0.0;
+            for (int64_t c = 0; c < n_ff; ++c) {
+                double hv = (double)q[j * n_ff + c] * (double)dsc[j * (n_ff / 32) + c / 32];
+                double p = row[c] * hv;
+                dd += p;
+                m += fabs(p);
+            }
+            double sc = (double)scales[j];
+            s += sc * dd;
+            a += fabs(sc) * m;
+        }
+        y[i * gin + r] = s;
+        if (absmag) absmag[i * gin + r] = a;
+        free(row);
+    }
+    (void)threads;
+    return bad ? -1 : 0;
+}
+
 /* Threads an OpenMP region would use (1 when built without OpenMP). */
 int oracle_max_threads(void) {
 #ifdef _OPENMP

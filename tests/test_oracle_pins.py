@@ -512,3 +512,29 @@ def test_moe_gate_up_q8_all_ones_weights():
     y, _ = oracle.moe_gate_up_q8("nvfp4", [mat, mat], scales, q, d, in_f, n_ff, n_used, t)
     s = sum(float(q[0, c]) * float(d[0, c // 32]) for c in range(in_f))
     assert np.allclose(y[0, 0], 0.75 * s, rtol=1e-15, atol=0) and np.allclose(y[1, 0], -1.5 * s, rtol=1e-15, atol=0)
+
+
+def test_moe_down_q8_equals_the_float_path_on_exact_activations():
+    import synth
+    # integer activations with +-127 in every block: d = 1 and q = h, so the
+    # Q8_1 down projection must equal the pinned float one exactly
+    n_ff, gin, n_used, t = 128, 8, 3, 2
+    n_pairs = n_used * t
+    rng = np.random.default_rng(6)
+    h = rng.integers(-127, 128, (n_pairs, n_ff)).astype(np.float32)
+    h[:, ::32] = -127.0
+    mats = [synth.nvfp4_rows(synth.nvfp4_matrix_seed(4, j, 2), gin, n_ff) for j in range(n_pairs)]
+    scales = np.array([0.5 + 0.01 * j for j in range(n_pairs)], np.float32)
+    q, d = oracle.quantize_q8_1(h, n_pairs, n_ff)
+    assert np.all(d == 1.0) and np.array_equal(q.astype(np.float32), h)
+    y8, a8 = oracle.moe_down_q8("nvfp4", mats, scales, q, d, n_ff, gin, n_used, t)
+    yf, af = oracle.moe_down("nvfp4", mats, scales, h, n_ff, gin, n_used, t)
+    assert np.array_equal(y8, yf) and np.array_equal(a8, af)
+    # a scale of 2 on one pair's blocks doubles that pair's share exactly
+    d2 = d.copy()
+    d2[1] = 2.0
+    y9, _ = oracle.moe_down_q8("nvfp4", mats, scales, q, d2, n_ff, gin, n_used, t)
+    h2 = h.copy()
+    h2[1] *= 2
+    yg, _ = oracle.moe_down("nvfp4", mats, scales, h2, n_ff, gin, n_used, t)
+    assert np.array_equal(y9, yg)

@@ -739,7 +739,6 @@ __global__ void __launch_bounds__(gr::THREADS, 1) gemv_rx_kernel(const gr::Param
         }
     }
     __syncthreads();
-    const int nunits = static_cast<int>((p.k + UW - 1) / UW);
     const float nan = __int_as_float(0x7FC00000);
 
     if (warp == COMPUTE_WARPS) {

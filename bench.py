@@ -9,10 +9,13 @@ the step's total algorithmic FLOPs (2*m*k*n per GEMM) over its device time.
 Inputs rotate over three copies (about 3 x 115 MB, more than the 129 MB L2), so
 every step reads its operands from HBM.
 
-The same run also times the small-batch GEMV (n = 1, 2, 4, 8 on 4608x1024 and
-1024x4608, Q4_K and Q8_0), the NVFP4 MoE gate/up GEMV (8 experts x 2 planes of
-2048x4096, four rotated weight copies) and the standalone dequant, and reports
-their weight-stream GB/s against the measured HBM bandwidth.
+The same run also times the k-quant prefill GEMMs (the same four shapes with W
+in Q4_K and Q6_K, a second step of eight calls), the small-batch GEMV (n = 1,
+2, 4, 8 on 4608x1024 and 1024x4608, Q4_K and Q8_0), the NVFP4 MoE gate/up GEMV
+(8 experts x 2 planes of 2048x4096, four rotated weight copies), the MoE down
+projection and the standalone dequant, and reports their GB/s (weight bytes,
+and all bytes moved) against the measured HBM bandwidth.  Every duration is
+the median over at least seven rounds.
 
 ``--impl reference`` times the f64 CPU oracle on a bounded sample of the same
 workload (this problem has no runnable reference implementation: the pages'
@@ -36,17 +39,20 @@ sys.path.insert(0, ROOT)
 
 METRIC = "quant-GEMM TFLOP/s per dtype (n=512 prefill); GEMV GB/s vs HBM peak"
 SHAPES = [("ffn_gate", 4608, 1024), ("ffn_down", 1024, 4608), ("conv_in", 3072, 1024), ("attn_out", 1024, 1024)]
-DTYPES = ["f32", "q4_0", "q8_0"]
+DTYPES = ["f32", "q4_0", "q8_0"]      # the headline step
+KQ_DTYPES = ["q4_k", "q6_k"]           # the k-quant step, timed beside it
 N_TOKENS = 512
+ROUNDS = 7
 COPIES = 3
-WORKLOAD = ("LFM2.5-350M 512-token prefill projections (ffn_gate 4608x1024, ffn_down 1024x4608, "
-            "conv_in 3072x1024, attn_out 1024x1024), W in f32/q4_0/q8_0, n=512")
+WORKLOAD = ("LFM2.5-350M 512-token prefill projections: ffn_gate 4608x1024, ffn_down 1024x4608, "
+            "conv_in 3072x1024, attn_out 1024x1024; W in f32, q4_0, q8_0; n=512")
 # nominal dense tensor-core rates (PFLOP/s): f16/bf16 2.25, tf32 1.1
 TF32_OVER_F16 = 1.1 / 2.25
 # DRAM bytes (read + write) per launch of the tensor-core GEMM kernel, the
-# mean over the step's 12 launches, from one ncu capture of this workload
-# (profiles/gemm_tc_kernel_step_dram_traffic.md).  It describes the kernel
-# sources it was taken on; if they change, the bench reports null.
+# mean over the step's 12 launches, from one ncu capture of this workload (the
+# dram__bytes_read.sum + dram__bytes_write.sum counters of every launch of one
+# step).  It describes the kernel sources it was taken on; if they change, the
+# bench reports null.
 GEMM_TRAFFIC_SOURCES = ("gemv_dequant_gemm_gb300/csrc/gemm_tc.cu", "gemv_dequant_gemm_gb300/csrc/decode.cuh",
                         "gemv_dequant_gemm_gb300/csrc/common.cuh")
 GEMM_TRAFFIC_SHA16 = "36d66afbb1831adc"
@@ -161,8 +167,9 @@ def _oracle_inputs():
     return ins
 
 
-def _oracle_sample(ins, entries_per_gemm, seed=0):
-    """Time the oracle on `entries_per_gemm` output entries of each GEMM."""
+def _oracle_sample(ins, entries_per_gemm, seed=0, threads=0):
+    """Time the oracle on `entries_per_gemm` output entries of each GEMM
+    (threads = 0: the OpenMP default, all host cores)."""
     import oracle
     rng = np.random.default_rng(seed)
     flops, t = 0.0, 0.0
@@ -170,14 +177,14 @@ def _oracle_sample(ins, entries_per_gemm, seed=0):
         ni = rng.integers(0, N_TOKENS, entries_per_gemm)
         mj = rng.integers(0, m, entries_per_gemm)
         t0 = time.perf_counter()
-        oracle.matmul_entries(fmt, w, x, m, k, N_TOKENS, ni, mj)
+        oracle.matmul_entries(fmt, w, x, m, k, N_TOKENS, ni, mj, threads=threads)
         t += time.perf_counter() - t0
         flops += 2.0 * k * entries_per_gemm
     return flops, t
 
 
-def _oracle_calibrate(ins, budget_s):
-    flops, t = _oracle_sample(ins, 64, seed=99)
+def _oracle_calibrate(ins, budget_s, threads=0):
+    flops, t = _oracle_sample(ins, 64, seed=99, threads=threads)
     per_entry_s = t / (64 * len(ins))
     return max(1, int(budget_s / (per_entry_s * len(ins))))
 
@@ -220,11 +227,126 @@ def run_reference(args):
 # GPU arm
 # --------------------------------------------------------------------------
 
+
+def _alg_bytes(q, fmt, m, k, n):
+    """Algorithmic bytes of one product: packed W, f32 X and f32 dst, each once."""
+    return m * q.qmm_row_bytes(fmt, k) + 4 * n * k + 4 * n * m
+
+
+def _med(xs):
+    return float(statistics.median(xs))
+
+
+def _build_gemms(q, torch, synth, dtypes, shapes, copies_n):
+    """Per GEMM: host arrays and `copies_n` rotated device copies of (W, X, dst, workspace)."""
+    gemms = []
+    for label, m, k in shapes:
+        x_np = synth.activations(N_TOKENS, k)
+        for fmt in dtypes:
+            w_np = synth.weights(fmt, m, k, m * q.qmm_row_bytes(fmt, k))
+            wsb = q.qmm_gemm_workspace_bytes(fmt, m, k, N_TOKENS)
+            copies = []
+            for _ in range(copies_n):
+                copies.append({
+                    "w": torch.from_numpy(w_np).cuda(), "x": torch.from_numpy(x_np).cuda(),
+                    "dst": torch.empty(N_TOKENS, m, dtype=torch.float32, device="cuda"),
+                    "ws": torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda"),
+                })
+            gemms.append({"label": label, "fmt": fmt, "m": m, "k": k, "wsb": wsb, "w_np": w_np, "x_np": x_np,
+                          "copies": copies, "flops": 2.0 * m * k * N_TOKENS,
+                          "bytes": _alg_bytes(q, fmt, m, k, N_TOKENS)})
+    return gemms
+
+
+class _Runner:
+    """Launches qmm_gemm for the GEMMs of a step through the C ABI."""
+
+    def __init__(self, q, lib, h, torch, stream, gemms, copies_n):
+        self.q, self.lib, self.h, self.torch, self.stream = q, lib, h, torch, stream
+        self.sptr = stream.cuda_stream
+        self.gemms, self.copies_n = gemms, copies_n
+
+    def launch(self, g, c):
+        b = g["copies"][c]
+        st = self.lib.qmm_gemm(self.h, self.q.DTYPES[g["fmt"]], b["w"].data_ptr(), b["x"].data_ptr(),
+                               b["dst"].data_ptr(), g["m"], g["k"], N_TOKENS,
+                               b["ws"].data_ptr() if g["wsb"] else None, g["wsb"], self.sptr)
+        if st:
+            raise self.q.QmmError(st, "qmm_gemm")
+
+    def step(self, c, evs=None):
+        for i, g in enumerate(self.gemms):
+            if evs is not None:
+                evs[i][0].record(self.stream)
+            self.launch(g, c)
+            if evs is not None:
+                evs[i][1].record(self.stream)
+
+    def warm(self, n):
+        for i in range(n):
+            self.step(i % self.copies_n)
+
+    def time_steps(self, steps):
+        """Device time (ms) of each of `steps` steps, each its GEMMs back to back.
+        A device-side sleep queued before each step keeps the GPU busy while
+        the host enqueues it, so the events time kernels, not launch gaps."""
+        torch = self.torch
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for s in range(steps):
+            torch.cuda._sleep(1_500_000)
+            evs[s][0].record(self.stream)
+            self.step(s % self.copies_n)
+            evs[s][1].record(self.stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    def time_calls(self, steps):
+        """Per-call durations [steps][gemm] (ms): an event pair around every
+        call, so these are single-call latencies (the events keep consecutive
+        calls from overlapping)."""
+        torch = self.torch
+        evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in self.gemms]
+               for _ in range(steps)]
+        for s in range(steps):
+            torch.cuda._sleep(1_500_000)
+            self.step(s % self.copies_n, evs[s])
+        torch.cuda.synchronize()
+        return np.array([[a.elapsed_time(b) for a, b in row] for row in evs])
+
+
+def _per_gemm(gemms, call_ms, f16_tflops, tf32_tflops, hbm_gbs):
+    """Per GEMM: median single-call time, TFLOP/s, and the fraction of its
+    roofline max(FLOPs at the tensor peak of its operand type, bytes at HBM)."""
+    out = []
+    for i, g in enumerate(gemms):
+        us = _med(call_ms[:, i]) * 1e3
+        peak = tf32_tflops if g["fmt"] == "f32" else f16_tflops
+        t_tensor = g["flops"] / (peak * 1e12)
+        t_hbm = g["bytes"] / (hbm_gbs * 1e9)
+        ideal = max(t_tensor, t_hbm)
+        out.append({"shape": g["label"], "dtype": g["fmt"], "us": round(us, 3),
+                    "tflops": round(g["flops"] / (us * 1e-6) / 1e12, 2),
+                    "bound": "tensor" if t_tensor >= t_hbm else "hbm",
+                    "ideal_us": round(ideal * 1e6, 3), "frac": round(ideal / (us * 1e-6), 4)})
+    return out
+
+
+def _per_dtype(gemms, call_ms, dtypes):
+    res = {}
+    for f in dtypes:
+        idx = [i for i, g in enumerate(gemms) if g["fmt"] == f]
+        if not idx:
+            continue
+        fl = sum(gemms[i]["flops"] for i in idx)
+        tt = sum(_med(call_ms[:, i]) for i in idx) * 1e-3
+        res[f] = round(fl / tt / 1e12, 2)
+    return res
+
+
 def run_ours(args):
     import torch
 
     import gemv_dequant_gemm_gb300 as q
-    import oracle
     import synth
 
     world, rank, local = _dist()
@@ -238,58 +360,25 @@ def run_ours(args):
     h = q.qmm_create(local)
     lib = q.load()
     stream = torch.cuda.current_stream()
-    sptr = stream.cuda_stream
 
     # ---- prefill workload: COPIES sets of (W, X, dst, workspace) ----
-    gemms = []  # per GEMM: dict with host arrays and per-copy device buffers
     copies_n = max(1, args.copies)
     shapes = [s for s in SHAPES if not args.only or s[0] in args.only.split(",")]
-    for label, m, k in shapes:
-        x_np = synth.activations(N_TOKENS, k)
-        for fmt in DTYPES:
-            w_np = synth.weights(fmt, m, k, m * q.qmm_row_bytes(fmt, k))
-            wsb = q.qmm_gemm_workspace_bytes(fmt, m, k, N_TOKENS)
-            copies = []
-            for c in range(copies_n):
-                copies.append({
-                    "w": torch.from_numpy(w_np).cuda(), "x": torch.from_numpy(x_np).cuda(),
-                    "dst": torch.empty(N_TOKENS, m, dtype=torch.float32, device="cuda"),
-                    "ws": torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda"),
-                })
-            gemms.append({"label": label, "fmt": fmt, "m": m, "k": k, "wsb": wsb, "w_np": w_np, "x_np": x_np,
-                          "copies": copies, "flops": 2.0 * m * k * N_TOKENS})
+    gemms = _build_gemms(q, torch, synth, DTYPES, shapes, copies_n)
+    run = _Runner(q, lib, h, torch, stream, gemms, copies_n)
     flops_step = sum(g["flops"] for g in gemms)
     copy_mb = sum(b.numel() * b.element_size() for g in gemms for b in g["copies"][0].values()) / 1e6
-    dt_code = {f: q.DTYPES[f] for f in DTYPES}
-
-    def launch(g, c):
-        b = g["copies"][c]
-        st = lib.qmm_gemm(h, dt_code[g["fmt"]], b["w"].data_ptr(), b["x"].data_ptr(), b["dst"].data_ptr(),
-                          g["m"], g["k"], N_TOKENS, b["ws"].data_ptr() if g["wsb"] else None, g["wsb"], sptr)
-        if st:
-            raise q.QmmError(st, "qmm_gemm")
-
-    def step(c, evs=None):
-        for i, g in enumerate(gemms):
-            if evs is not None:
-                evs[i][0].record(stream)
-            launch(g, c)
-            if evs is not None:
-                evs[i][1].record(stream)
 
     # launches of our kernels per step: x->f16 + tensor-core GEMM for packed W, one for f32 W
     # (all launched with programmatic dependent launch, so consecutive calls overlap)
     launches_per_step = sum(1 if g["fmt"] == "f32" else 2 for g in gemms)
 
-    for i in range(args.warmup):
-        step(i % copies_n)
+    run.warm(args.warmup)
     torch.cuda.synchronize()
     if q.qmm_sync_status(h) != 0:
         raise RuntimeError("device status set during warm-up")
 
     # ---- timed region: K steps, each its 12 GEMMs back to back ----
-    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
@@ -297,14 +386,7 @@ def run_ours(args):
     clocks = ClockSampler(local)
     time.sleep(0.25)
     wall0 = time.perf_counter()
-    for s in range(args.steps):
-        # keep the GPU busy while the host enqueues the step, so the events
-        # below time kernels and not host launch gaps
-        torch.cuda._sleep(1_500_000)
-        ev_step[s][0].record(stream)
-        step(s % copies_n)
-        ev_step[s][1].record(stream)
-    torch.cuda.synchronize()
+    step_ms = run.time_steps(args.steps)
     wall = time.perf_counter() - wall0
     clk = clocks.stop()
     if world > 1:
@@ -313,44 +395,53 @@ def run_ours(args):
     status = q.qmm_sync_status(h)
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
-    step_ms = [a.elapsed_time(b) for a, b in ev_step]
     # per-GEMM durations: the same steps with an event pair around every call
-    # (events serialize the calls, so these are single-call latencies)
-    kb = max(3, min(100, args.steps))
-    ev_launch = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in gemms]
-                 for _ in range(kb)]
-    for s in range(kb):
-        torch.cuda._sleep(1_500_000)
-        step(s % copies_n, ev_launch[s])
-    torch.cuda.synchronize()
-    launch_ms = np.array([[a.elapsed_time(b) for a, b in row] for row in ev_launch])  # [steps][gemm]
-    ms_per_step = slowest_rank_ms(float(np.mean(step_ms)), world, "cuda")
+    kb = max(ROUNDS, min(100, args.steps))
+    call_ms = run.time_calls(kb)
+    ms_per_step = slowest_rank_ms(_med(step_ms), world, "cuda")
     value = job_tflops(world, flops_step, ms_per_step)
 
-    per_gemm = []
-    for i, g in enumerate(gemms):
-        us = float(np.mean(launch_ms[:, i])) * 1e3
-        peak = tf32_tflops if g["fmt"] == "f32" else f16_tflops
-        per_gemm.append({"shape": g["label"], "dtype": g["fmt"], "us": round(us, 3),
-                         "tflops": round(g["flops"] / (us * 1e-6) / 1e12, 2),
-                         "frac": round(g["flops"] / (us * 1e-6) / 1e12 / peak, 4)})
-    per_dtype = {}
-    for f in DTYPES:
-        idx = [i for i, g in enumerate(gemms) if g["fmt"] == f]
-        fl = sum(gemms[i]["flops"] for i in idx)
-        tt = sum(float(np.mean(launch_ms[:, i])) for i in idx) * 1e-3
-        per_dtype[f] = round(fl / tt / 1e12, 2)
-    # dominant kernel: the tensor-core GEMM (qmm_gemm, n=512), all its launches;
-    # its peak is the FLOP-weighted harmonic mix of the f16 and tf32 peaks
-    tot_t = float(np.sum(np.mean(launch_ms, axis=0))) * 1e-3
-    ideal_t = sum(g["flops"] / ((tf32_tflops if g["fmt"] == "f32" else f16_tflops) * 1e12) for g in gemms)
+    per_gemm = _per_gemm(gemms, call_ms, f16_tflops, tf32_tflops, hbm_gbs)
+    per_dtype = _per_dtype(gemms, call_ms, DTYPES)
+    # dominant kernel: the tensor-core GEMM (qmm_gemm, n=512), all its launches.
+    # Its roofline is per GEMM max(FLOPs at the tensor peak of its operand
+    # type, algorithmic bytes at HBM); `peak` is the step's FLOPs over the sum
+    # of those ideal times, so frac = sum(ideal) / sum(measured).
+    tot_t = sum(_med(call_ms[:, i]) for i in range(len(gemms))) * 1e-3
+    ideal_t = sum(p["ideal_us"] for p in per_gemm) * 1e-6
     achieved = flops_step / tot_t / 1e12
-    peak_mix = flops_step / ideal_t / 1e12
-    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak_mix, 1), "unit": "TFLOP/s",
-                "frac": round(achieved / peak_mix, 4), "traffic": _gemm_traffic(),
+    peak_eff = flops_step / ideal_t / 1e12
+    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak_eff, 1), "unit": "TFLOP/s",
+                "frac": round(achieved / peak_eff, 4), "traffic": _gemm_traffic(),
                 "traffic_unit": "bytes per gemm_tc_kernel launch (DRAM read + write, ncu)",
-                "kernel": "qmm_gemm tensor-core path (x_to_f16 + gemm_tc); per-call event-timed durations",
-                "peak_source": f"{peak_src} bf16 dense {f16_tflops} TFLOP/s; tf32 = x{TF32_OVER_F16:.3f} nominal"}
+                "kernel": "qmm_gemm tensor-core path (x_to_f16 + gemm_tc); per-call event-timed durations, "
+                          f"median of {kb} steps",
+                "peak_source": f"{peak_src}: bf16 dense {f16_tflops} TFLOP/s (f16 operands), tf32 = "
+                               f"x{TF32_OVER_F16:.3f} nominal ratio, HBM {hbm_gbs} GB/s; per GEMM the slower of "
+                               "FLOPs at its tensor peak and algorithmic bytes at HBM"}
+
+    # ---- the k-quant step (config 2): the same shapes with W in Q4_K / Q6_K ----
+    kquant = None
+    if not args.no_kquant:
+        try:
+            kq = _build_gemms(q, torch, synth, KQ_DTYPES, shapes, copies_n)
+            krun = _Runner(q, lib, h, torch, stream, kq, copies_n)
+            krun.warm(max(3, args.warmup // 4))
+            ksteps = max(ROUNDS, min(200, args.steps))
+            kstep_ms = krun.time_steps(ksteps)
+            kcall_ms = krun.time_calls(max(ROUNDS, min(100, args.steps)))
+            if q.qmm_sync_status(h) != 0:
+                raise RuntimeError("device status set in the k-quant step")
+            kflops = sum(g["flops"] for g in kq)
+            kpg = _per_gemm(kq, kcall_ms, f16_tflops, tf32_tflops, hbm_gbs)
+            per_gemm += kpg
+            per_dtype.update(_per_dtype(kq, kcall_ms, KQ_DTYPES))
+            kquant = {"gemms": len(kq), "steps": ksteps, "ms_per_step": round(_med(kstep_ms), 5),
+                      "tflops": round(kflops / (_med(kstep_ms) * 1e-3) / 1e12, 2),
+                      "frac": round(sum(p["ideal_us"] for p in kpg) / (sum(p["us"] for p in kpg)), 4)}
+            del kq, krun
+        except Exception as exc:  # reported in the JSON line, never fatal to the headline measurement
+            kquant = {"error": f"{type(exc).__name__}: {exc}"}
 
     # ---- e2e: host buffers through the public API ----
     e2e = None
@@ -372,7 +463,7 @@ def run_ours(args):
                     b = g["copies"][c]
                     b["w"].copy_(p["w"], non_blocking=True)
                     b["x"].copy_(p["x"], non_blocking=True)
-                    launch(g, c)
+                    run.launch(g, c)
                     p["dst"].copy_(b["dst"], non_blocking=True)
             ev1.record(stream)
             torch.cuda.synchronize()
@@ -380,17 +471,24 @@ def run_ours(args):
         e2e = {"value": round(job_tflops(world, flops_step, e2e_ms), 3), "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 4)}
 
-    # ---- a6-a8: GEMV, MoE, dequant (weight-stream GB/s vs HBM) ----
+    # ---- a6-a8, f1-f3: GEMV, MoE, dequant (GB/s vs HBM) ----
     sub = None if args.no_sub else run_sub_benches(q, lib, h, torch, synth, stream, hbm_gbs)
 
-    # ---- CPU baseline: the oracle on a bounded sample ----
+    # ---- CPU baseline: the oracle on a bounded sample, all cores and one core ----
     cpu = None
     if rank == 0 and not args.no_cpu:
         ins = _oracle_inputs()
-        entries = _oracle_calibrate(ins, 15.0)
-        f, t = _oracle_sample(ins, entries, seed=7)
-        cpu = {"value": f / t / 1e12, "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
-               "sample": f"{entries} random output entries of each of the 12 GEMMs (f64 oracle, {t:.1f} s)"}
+        cores = _cores()  # before any one-thread run changes the OpenMP default
+        entries = _oracle_calibrate(ins, 12.0, threads=cores)
+        f, t = _oracle_sample(ins, entries, seed=7, threads=cores)
+        entries1 = _oracle_calibrate(ins, 6.0, threads=1)
+        f1, t1 = _oracle_sample(ins, entries1, seed=8, threads=1)
+        cpu = {"value": f / t / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": f"{entries} random output entries of each of the 12 GEMMs (f64 oracle, OpenMP, {t:.1f} s)",
+               "single_thread": {"value": f1 / t1 / 1e12, "unit": "TFLOP/s", "cores": 1,
+                                 "sample": f"{entries1} random output entries of each of the 12 GEMMs "
+                                           f"(f64 oracle, one thread, {t1:.1f} s)"},
+               "cpu": _cpu_model()}
 
     q.qmm_destroy(h)
     if rank == 0:
@@ -401,9 +499,11 @@ def run_ours(args):
             "data": "synthetic (seeded LCG / xorshift64 streams)",
             "config": {"workload": WORKLOAD, "n": N_TOKENS, "dtypes": DTYPES,
                        "gemms_per_step": len(gemms), "flops_per_step": flops_step,
+                       "timing": f"median of {args.steps} per-step event pairs; mean "
+                                 f"{float(np.mean(step_ms)):.5f} ms",
                        "l2": f"inputs rotated over {copies_n} copies of {copy_mb:.0f} MB (L2 129 MB)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-            "per_dtype_tflops": per_dtype, "per_gemm": per_gemm, "roofline": roofline,
+            "per_dtype_tflops": per_dtype, "per_gemm": per_gemm, "kquant_step": kquant, "roofline": roofline,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
             "clocks": clk, "timed_wall_s": round(wall, 3), "sub": sub,
         }
@@ -414,27 +514,47 @@ def run_ours(args):
     return 0
 
 
-def _time_calls(torch, stream, calls, reps):
-    """Mean device time (ms) per call of calls[i % len(calls)]() over reps
-    back-to-back launches: one event pair around the whole run, so that the
-    launches overlap as they do in a model's stream (programmatic dependent
-    launch) and no per-call event splits them.  A device-side sleep queued
-    first keeps the GPU busy while the host enqueues the run."""
+def _cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
+
+
+def _time_calls(torch, stream, calls, reps, rounds=ROUNDS):
+    """Device time (ms) per call of calls[i % len(calls)]() over `reps`
+    back-to-back launches, one event pair around each round of `reps` calls
+    (so the launches overlap as they do in a model's stream, programmatic
+    dependent launch included, and no per-call event splits them); the
+    median over `rounds` rounds, with the smallest and largest.  A
+    device-side sleep queued before each round keeps the GPU busy while the
+    host enqueues it."""
     for i in range(min(reps, 3)):
         calls[i % len(calls)]()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        torch.cuda._sleep(max(2_000_000, 20_000 * reps))
-    e0.record(stream)
-    for i in range(reps):
-        calls[i % len(calls)]()
-    e1.record(stream)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(rounds)]
+    for r in range(rounds):
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(max(2_000_000, 20_000 * reps))
+        evs[r][0].record(stream)
+        for i in range(reps):
+            calls[(r * reps + i) % len(calls)]()
+        evs[r][1].record(stream)
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / reps
+    per = [a.elapsed_time(b) / reps for a, b in evs]
+    return _med(per), min(per), max(per)
 
 
-def _moe_v2_sub(q, lib, h, torch, stream, keep, scales, x, y, in_f, n_ff, n_used, n_pairs, wbytes, hbm_gbs):
+def _rate(label_bytes, ms, hbm_gbs):
+    gbs = label_bytes / (ms * 1e-3) / 1e9
+    return round(gbs, 1), round(gbs / hbm_gbs, 4)
+
+
+def _moe_v2_sub(q, lib, h, torch, stream, keep, scales, x, y, in_f, n_ff, n_used, n_pairs, wbytes, tbytes, hbm_gbs):
     sptr = stream.cuda_stream
     mat_bytes = n_ff * q.qmm_row_bytes("nvfp4", in_f)
     keep2, tables2 = [], []
@@ -453,24 +573,54 @@ def _moe_v2_sub(q, lib, h, torch, stream, keep, scales, x, y, in_f, n_ff, n_used
                                              y.data_ptr(), in_f, n_ff, n_used, 1, sptr)) for tb in tables2]
     if calls[0]() != 0:
         raise RuntimeError("qmm_moe_gemv refused the V2 table")
-    ms = _time_calls(torch, stream, calls, 40)
-    gbs = wbytes / (ms * 1e-3) / 1e9
-    moe_v2 = {"us": round(ms * 1e3, 3), "weight_bytes": wbytes, "weight_gbs": round(gbs, 1),
-              "frac_hbm": round(gbs / hbm_gbs, 4)}
+    ms, lo, hi = _time_calls(torch, stream, calls, 40)
+    wg, wf = _rate(wbytes, ms, hbm_gbs)
+    tg, tf = _rate(tbytes, ms, hbm_gbs)
+    moe_v2 = {"us": round(ms * 1e3, 3), "us_min": round(lo * 1e3, 3), "us_max": round(hi * 1e3, 3),
+              "weight_bytes": wbytes, "weight_gbs": wg, "frac_hbm": wf, "total_bytes": tbytes, "total_gbs": tg,
+              "frac_hbm_total": tf}
     pairs = list(zip(keep, keep2))
     calls = [(lambda s=s_, d=d_: lib.qmm_nvfp4_repack_v2(h, s.data_ptr(), d.data_ptr(), n_ff, in_f, sptr))
              for s_, d_ in pairs]
-    ms = _time_calls(torch, stream, calls, len(calls))
-    gbs = 2 * mat_bytes / (ms * 1e-3) / 1e9
-    repack = {"m": n_ff, "k": in_f, "us": round(ms * 1e3, 3), "bytes": 2 * mat_bytes, "gbs": round(gbs, 1),
-              "frac_hbm": round(gbs / hbm_gbs, 4)}
+    ms, lo, hi = _time_calls(torch, stream, calls, len(calls))
+    g, f = _rate(2 * mat_bytes, ms, hbm_gbs)
+    repack = {"m": n_ff, "k": in_f, "us": round(ms * 1e3, 3), "bytes": 2 * mat_bytes, "gbs": g, "frac_hbm": f}
     del keep2, tables2
     return moe_v2, repack
 
 
+def _moe_q8_sub(q, lib, h, torch, stream, tables, scales, x, in_f, n_ff, n_used, n_pairs, wbytes, hbm_gbs):
+    sptr = stream.cuda_stream
+    qd = torch.empty(1, in_f, dtype=torch.int8, device="cuda")
+    dd = torch.empty(1, in_f // 32, dtype=torch.float32, device="cuda")
+    y = torch.empty(2, n_pairs, n_ff, dtype=torch.float32, device="cuda")
+
+    def quant():
+        return lib.qmm_quantize_q8_1(h, x.data_ptr(), qd.data_ptr(), dd.data_ptr(), 1, in_f, sptr)
+
+    def gemv(tb):
+        return lib.qmm_moe_gemv_q8(h, q.NVFP4, tb.data_ptr(), scales.data_ptr(), qd.data_ptr(), dd.data_ptr(),
+                                   y.data_ptr(), in_f, n_ff, n_used, 1, sptr)
+    if quant() != 0 or gemv(tables[0]) != 0:
+        raise RuntimeError("qmm_quantize_q8_1 / qmm_moe_gemv_q8 refused the call")
+    res = {}
+    for label, calls, launches in (
+            ("with_quantize", [(lambda tb=tb: quant() or gemv(tb)) for tb in tables], 2),
+            ("kernel_only", [(lambda tb=tb: gemv(tb)) for tb in tables], 1)):
+        ms, lo, hi = _time_calls(torch, stream, calls, 40)
+        wg, wf = _rate(wbytes, ms, hbm_gbs)
+        res[label] = {"us": round(ms * 1e3, 3), "us_min": round(lo * 1e3, 3), "us_max": round(hi * 1e3, 3),
+                      "weight_gbs": wg, "frac_hbm": wf, "launches_per_call": launches}
+    res["weight_bytes"] = wbytes
+    return res
+
+
 def run_sub_benches(q, lib, h, torch, synth, stream, hbm_gbs):
     sptr = stream.cuda_stream
-    out = {"gemv": [], "moe": None, "moe_v2": None, "repack_v2": None, "moe_down": None, "dequant": []}
+    out = {"timing": f"median over {ROUNDS} rounds of back-to-back calls (weights rotated through more "
+                     "than 2x the L2 size)",
+           "gemv": [], "moe": None, "moe_q8": None, "moe_v2": None, "repack_v2": None, "moe_down": None,
+           "moe_down_q8": None, "dequant": []}
     # GEMV: rotate over enough weight copies to exceed L2 several times
     for fmt in ("q4_k", "q8_0"):
         for m, k in ((4608, 1024), (1024, 4608)):
@@ -484,10 +634,13 @@ def run_sub_benches(q, lib, h, torch, synth, stream, hbm_gbs):
                 d = torch.empty(n, m, dtype=torch.float32, device="cuda")
                 calls = [(lambda wt=wt: lib.qmm_gemv(h, q.DTYPES[fmt], wt.data_ptr(), x.data_ptr(), d.data_ptr(),
                                                      m, k, n, sptr)) for wt in ws]
-                ms = _time_calls(torch, stream, calls, 2 * ncopy)
-                gbs = wbytes / (ms * 1e-3) / 1e9
+                ms, lo, hi = _time_calls(torch, stream, calls, ncopy)
+                tbytes = _alg_bytes(q, fmt, m, k, n)
+                wg, wf = _rate(wbytes, ms, hbm_gbs)
+                tg, tf = _rate(tbytes, ms, hbm_gbs)
                 out["gemv"].append({"dtype": fmt, "m": m, "k": k, "n": n, "us": round(ms * 1e3, 3),
-                                    "weight_gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm_gbs, 4)})
+                                    "us_min": round(lo * 1e3, 3), "us_max": round(hi * 1e3, 3),
+                                    "weight_gbs": wg, "frac_hbm": wf, "total_gbs": tg, "frac_hbm_total": tf})
             del ws
     # MoE gate/up: 8 experts x {gate, up}, 4 rotated copies of the weight set
     in_f, n_ff, n_used = 4096, 2048, 8
@@ -507,16 +660,26 @@ def run_sub_benches(q, lib, h, torch, synth, stream, hbm_gbs):
     y = torch.empty(2, n_pairs, n_ff, dtype=torch.float32, device="cuda")
     calls = [(lambda tb=tb: lib.qmm_moe_gemv(h, q.NVFP4, tb.data_ptr(), scales.data_ptr(), x.data_ptr(),
                                              y.data_ptr(), in_f, n_ff, n_used, 1, sptr)) for tb in tables]
-    ms = _time_calls(torch, stream, calls, 40)
+    ms, lo, hi = _time_calls(torch, stream, calls, 40)
     wbytes = 2 * n_pairs * n_ff * rb
-    gbs = wbytes / (ms * 1e-3) / 1e9
-    out["moe"] = {"us": round(ms * 1e3, 3), "weight_bytes": wbytes, "weight_gbs": round(gbs, 1),
-                  "frac_hbm": round(gbs / hbm_gbs, 4)}
+    tbytes = wbytes + 4 * in_f + 2 * n_pairs * n_ff * 4 + 2 * n_pairs * (8 + 4)
+    wg, wf = _rate(wbytes, ms, hbm_gbs)
+    tg, tf = _rate(tbytes, ms, hbm_gbs)
+    out["moe"] = {"us": round(ms * 1e3, 3), "us_min": round(lo * 1e3, 3), "us_max": round(hi * 1e3, 3),
+                  "weight_bytes": wbytes, "weight_gbs": wg, "frac_hbm": wf, "total_bytes": tbytes,
+                  "total_gbs": tg, "frac_hbm_total": tf}
+    # the same products on int8 (Q8_1) activations: the quantizer and the
+    # dp4a kernel, two launches per call, and the kernel alone
+    try:
+        out["moe_q8"] = _moe_q8_sub(q, lib, h, torch, stream, tables, scales, x, in_f, n_ff, n_used, n_pairs,
+                                    wbytes, hbm_gbs)
+    except Exception as exc:  # reported in the JSON line, never fatal to the headline measurement
+        out["moe_q8"] = {"error": f"{type(exc).__name__}: {exc}"}
     # the same call on V2 rows (codes, then the scale stream) made by the
     # library's repack, and the repack itself (read + write of each matrix)
     try:
         out["moe_v2"], out["repack_v2"] = _moe_v2_sub(q, lib, h, torch, stream, keep, scales, x, y, in_f, n_ff,
-                                                      n_used, n_pairs, wbytes, hbm_gbs)
+                                                      n_used, n_pairs, wbytes, tbytes, hbm_gbs)
     except Exception as exc:  # reported in the JSON line, never fatal to the headline measurement
         out["moe_v2"] = {"error": f"{type(exc).__name__}: {exc}"}
     del keep, tables
@@ -539,24 +702,46 @@ def run_sub_benches(q, lib, h, torch, synth, stream, hbm_gbs):
     calls = [(lambda tb=tb: lib.qmm_moe_down(h, q.NVFP4, tb.data_ptr(), scales.data_ptr(), hact.data_ptr(),
                                              yd.data_ptr(), n_ff_d, gin, n_used, 1, ws.data_ptr(), wsb, sptr))
              for tb in tables]
-    ms = _time_calls(torch, stream, calls, 48)
+    ms, lo, hi = _time_calls(torch, stream, calls, 48)
     wbytes = n_pairs * gin * rb
-    gbs = wbytes / (ms * 1e-3) / 1e9
-    out["moe_down"] = {"us": round(ms * 1e3, 3), "weight_bytes": wbytes, "weight_gbs": round(gbs, 1),
-                       "frac_hbm": round(gbs / hbm_gbs, 4), "launches_per_call": 2}
+    # + activations, the per-pair products written and read back, y
+    tbytes = wbytes + 4 * n_pairs * n_ff_d + 2 * 4 * n_pairs * gin + 4 * gin
+    wg, wf = _rate(wbytes, ms, hbm_gbs)
+    tg, tf = _rate(tbytes, ms, hbm_gbs)
+    out["moe_down"] = {"us": round(ms * 1e3, 3), "us_min": round(lo * 1e3, 3), "us_max": round(hi * 1e3, 3),
+                       "weight_bytes": wbytes, "weight_gbs": wg, "frac_hbm": wf, "total_bytes": tbytes,
+                       "total_gbs": tg, "frac_hbm_total": tf, "launches_per_call": 2}
+    try:  # on int8 (Q8_1) activations: quantizer, dp4a kernel, combine
+        qd = torch.empty(n_pairs, n_ff_d, dtype=torch.int8, device="cuda")
+        dd = torch.empty(n_pairs, n_ff_d // 32, dtype=torch.float32, device="cuda")
+
+        def down_q8(tb):
+            st = lib.qmm_quantize_q8_1(h, hact.data_ptr(), qd.data_ptr(), dd.data_ptr(), n_pairs, n_ff_d, sptr)
+            return st or lib.qmm_moe_down_q8(h, q.NVFP4, tb.data_ptr(), scales.data_ptr(), qd.data_ptr(),
+                                             dd.data_ptr(), yd.data_ptr(), n_ff_d, gin, n_used, 1, ws.data_ptr(),
+                                             wsb, sptr)
+        calls = [(lambda tb=tb: down_q8(tb)) for tb in tables]
+        if calls[0]() != 0:
+            raise RuntimeError("qmm_moe_down_q8 refused the call")
+        ms, lo, hi = _time_calls(torch, stream, calls, 48)
+        wg, wf = _rate(wbytes, ms, hbm_gbs)
+        out["moe_down_q8"] = {"us": round(ms * 1e3, 3), "us_min": round(lo * 1e3, 3), "us_max": round(hi * 1e3, 3),
+                              "weight_bytes": wbytes, "weight_gbs": wg, "frac_hbm": wf, "launches_per_call": 3}
+    except Exception as exc:
+        out["moe_down_q8"] = {"error": f"{type(exc).__name__}: {exc}"}
     del keep, tables
     # dequant: read packed + write f32
-    for fmt, m, k in (("q4_k", 4608, 1024), ("q6_k", 4608, 1024), ("nvfp4", 2048, 4096)):
+    for fmt, m, k in (("q4_0", 4608, 1024), ("q8_0", 4608, 1024), ("q4_k", 4608, 1024), ("q6_k", 4608, 1024),
+                      ("nvfp4", 2048, 4096)):
         rb = q.qmm_row_bytes(fmt, k)
         w = torch.from_numpy(synth.weights(fmt, m, k, m * rb)).cuda()
         outs = [torch.empty(m, k, dtype=torch.float32, device="cuda") for _ in range(8)]
         calls = [(lambda o=o: lib.qmm_dequant(h, q.DTYPES[fmt], w.data_ptr(), o.data_ptr(), m, k,
                                               1.0, sptr)) for o in outs]
-        ms = _time_calls(torch, stream, calls, 32)
+        ms, lo, hi = _time_calls(torch, stream, calls, 32)
         tot = m * rb + 4 * m * k
-        gbs = tot / (ms * 1e-3) / 1e9
-        out["dequant"].append({"dtype": fmt, "m": m, "k": k, "us": round(ms * 1e3, 3), "gbs": round(gbs, 1),
-                               "frac_hbm": round(gbs / hbm_gbs, 4)})
+        g, f = _rate(tot, ms, hbm_gbs)
+        out["dequant"].append({"dtype": fmt, "m": m, "k": k, "us": round(ms * 1e3, 3), "gbs": g, "frac_hbm": f})
         if fmt == "nvfp4":  # the same rows as V2 (codes, then the scale stream), made by the library's repack
             try:
                 w2 = torch.empty_like(w)
@@ -564,16 +749,70 @@ def run_sub_benches(q, lib, h, torch, synth, stream, hbm_gbs):
                     raise RuntimeError("qmm_nvfp4_repack_v2 refused the call")
                 calls = [(lambda o=o: lib.qmm_dequant(h, q.NVFP4_V2, w2.data_ptr(), o.data_ptr(), m, k,
                                                       1.0, sptr)) for o in outs]
-                ms = _time_calls(torch, stream, calls, 32)
-                gbs = tot / (ms * 1e-3) / 1e9
-                out["dequant"].append({"dtype": "nvfp4_v2", "m": m, "k": k, "us": round(ms * 1e3, 3),
-                                       "gbs": round(gbs, 1), "frac_hbm": round(gbs / hbm_gbs, 4)})
+                ms, lo, hi = _time_calls(torch, stream, calls, 32)
+                g, f = _rate(tot, ms, hbm_gbs)
+                out["dequant"].append({"dtype": "nvfp4_v2", "m": m, "k": k, "us": round(ms * 1e3, 3), "gbs": g,
+                                       "frac_hbm": f})
             except Exception as exc:
                 out["dequant"].append({"dtype": "nvfp4_v2", "error": f"{type(exc).__name__}: {exc}"})
     st = q.qmm_sync_status(h)
     if st != 0:
         raise RuntimeError(f"device status {st} in the sub-benchmarks")
     return out
+
+
+def run_profile_gemv(args):
+    """One GEMV shape called back to back (a profiling run: not a bench line)."""
+    import torch
+
+    import gemv_dequant_gemm_gb300 as q
+    import synth
+    fmt, m, k, n = args.profile_gemv.split(",")
+    m, k, n = int(m), int(k), int(n)
+    torch.cuda.set_device(0)
+    h = q.qmm_create(0)
+    w = torch.from_numpy(synth.weights(fmt, m, k, m * q.qmm_row_bytes(fmt, k))).cuda()
+    x = torch.from_numpy(synth.activations(n, k)).cuda()
+    d = torch.empty(n, m, dtype=torch.float32, device="cuda")
+    for _ in range(args.steps + args.warmup):
+        q.qmm_gemv(h, fmt, w, x, d, m, k, n)
+    torch.cuda.synchronize()
+    st = q.qmm_sync_status(h)
+    q.qmm_destroy(h)
+    print(json.dumps({"profile_gemv": args.profile_gemv, "calls": args.steps + args.warmup, "status": st}))
+    return 0 if st == 0 else 1
+
+
+def run_profile_moe(args):
+    """The NVFP4 MoE gate/up call (f32 or Q8_1 activations) on one weight set,
+    called back to back (a profiling run: not a bench line)."""
+    import torch
+
+    import gemv_dequant_gemm_gb300 as q
+    import synth
+    mode = args.profile_moe
+    in_f, n_ff, n_used = 4096, 2048, 8
+    torch.cuda.set_device(0)
+    h = q.qmm_create(0)
+    mats = [torch.from_numpy(synth.nvfp4_rows(synth.nvfp4_matrix_seed(0, j, p), n_ff, in_f)).cuda()
+            for p in range(2) for j in range(n_used)]
+    table = torch.tensor([m.data_ptr() for m in mats], dtype=torch.int64, device="cuda")
+    scales = torch.tensor([0.5 + 0.01 * i for i in range(2 * n_used)], dtype=torch.float32, device="cuda")
+    x = torch.from_numpy(synth.activations(1, in_f)).cuda()
+    y = torch.empty(2, n_used, n_ff, dtype=torch.float32, device="cuda")
+    qd = torch.empty(1, in_f, dtype=torch.int8, device="cuda")
+    dd = torch.empty(1, in_f // 32, dtype=torch.float32, device="cuda")
+    for _ in range(args.steps + args.warmup):
+        if mode == "q8":
+            q.qmm_quantize_q8_1(h, x, qd, dd, 1, in_f)
+            q.qmm_moe_gemv_q8(h, "nvfp4", table, scales, qd, dd, y, in_f, n_ff, n_used, 1)
+        else:
+            q.qmm_moe_gemv(h, "nvfp4", table, scales, x, y, in_f, n_ff, n_used, 1)
+    torch.cuda.synchronize()
+    st = q.qmm_sync_status(h)
+    q.qmm_destroy(h)
+    print(json.dumps({"profile_moe": mode, "calls": args.steps + args.warmup, "status": st}))
+    return 0 if st == 0 else 1
 
 
 def main(argv=None):
@@ -583,15 +822,24 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sub", action="store_true", help="skip the GEMV / MoE / dequant sub-benchmarks")
+    ap.add_argument("--no-kquant", action="store_true", help="skip the Q4_K / Q6_K prefill step")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--only", default=None,
                     help="comma-separated shape labels to keep (profiling runs; not a headline workload)")
     ap.add_argument("--copies", type=int, default=COPIES,
                     help="rotated input copies (profiling runs use 1 to keep the device footprint small)")
+    ap.add_argument("--profile-gemv", default=None, metavar="FMT,M,K,N",
+                    help="call one GEMV shape warmup+steps times and exit (profiling runs)")
+    ap.add_argument("--profile-moe", default=None, choices=["f32", "q8"],
+                    help="call the NVFP4 MoE gate/up (f32 or Q8_1 activations) warmup+steps times and exit")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.profile_gemv:
+        return run_profile_gemv(args)
+    if args.profile_moe:
+        return run_profile_moe(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -6,7 +6,8 @@ status codes into exceptions.  There is no fallback: if the library cannot be
 loaded, importing the functions raises.
 
 Names follow the C ABI: ``qmm_create``, ``qmm_destroy``, ``qmm_gemm``,
-``qmm_gemv``, ``qmm_moe_gemv``, ``qmm_moe_down``, ``qmm_nvfp4_repack_v2``, ``qmm_dequant``, ``qmm_sync_status``,
+``qmm_gemv``, ``qmm_moe_gemv``, ``qmm_moe_down``, ``qmm_quantize_q8_1``, ``qmm_moe_gemv_q8``,
+``qmm_moe_down_q8``, ``qmm_nvfp4_repack_v2``, ``qmm_dequant``, ``qmm_sync_status``,
 ``qmm_row_bytes``, ``qmm_gemm_workspace_bytes``, ``qmm_moe_down_workspace_bytes``,
 ``qmm_strerror``.
 """
@@ -30,8 +31,10 @@ STATUS = {0: "QMM_OK", 1: "QMM_ERR_INVALID_ARG", 2: "QMM_ERR_UNSUPPORTED", 3: "Q
 # Every symbol include/qmm.h and include/qmm_testing.h declare.
 EXPORTS = ("qmm_create", "qmm_destroy", "qmm_strerror", "qmm_block_weights", "qmm_block_bytes",
            "qmm_row_bytes", "qmm_gemm_workspace_bytes", "qmm_gemm", "qmm_gemv", "qmm_moe_gemv",
-           "qmm_moe_down_workspace_bytes", "qmm_moe_down", "qmm_nvfp4_repack_v2",
-           "qmm_dequant", "qmm_sync_status", "qmm_gemm_noalloc", "qmm_testing_set_wait_limit_ns",
+           "qmm_moe_down_workspace_bytes", "qmm_moe_down", "qmm_nvfp4_repack_v2", "qmm_quantize_q8_1",
+           "qmm_moe_gemv_q8", "qmm_moe_down_q8",
+           "qmm_dequant", "qmm_sync_status", "qmm_gemm_noalloc", "qmm_gemm_noalloc_status",
+           "qmm_testing_set_wait_limit_ns",
            "qmm_testing_skip_first_stage_load")
 
 
@@ -70,9 +73,13 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "qmm_moe_down_workspace_bytes": (SZ, [I64, I, I]),
         "qmm_moe_down": (I, [P, I, P, P, P, P, I64, I64, I, I, P, SZ, P]),
         "qmm_dequant": (I, [P, I, P, P, I64, I64, ctypes.c_float, P]),
+        "qmm_quantize_q8_1": (I, [P, P, P, P, I64, I64, P]),
+        "qmm_moe_gemv_q8": (I, [P, I, P, P, P, P, P, I64, I64, I, I, P]),
+        "qmm_moe_down_q8": (I, [P, I, P, P, P, P, P, I64, I64, I, I, P, SZ, P]),
         "qmm_nvfp4_repack_v2": (I, [P, P, P, I64, I64, P]),
         "qmm_sync_status": (I, [P, P]),
         "qmm_gemm_noalloc": (I, [I, P, P, P, I64, I64, I64, P]),
+        "qmm_gemm_noalloc_status": (I, [P]),
         "qmm_testing_set_wait_limit_ns": (I, [P, ctypes.c_uint64]),
         "qmm_testing_skip_first_stage_load": (I, [P, I]),
     }
@@ -178,6 +185,27 @@ def qmm_moe_down(h, t, w_ptrs, scales, hact, y, n_ff, gin, n_used, t_tokens, wor
                                t_tokens, _ptr(workspace), workspace_bytes, _stream(stream)), "qmm_moe_down")
 
 
+Q8_MAX_K = 8192
+
+
+def qmm_quantize_q8_1(h, x, q, d, rows, k, stream=None) -> None:
+    _check(load().qmm_quantize_q8_1(h, _ptr(x), _ptr(q), _ptr(d), rows, k, _stream(stream)), "qmm_quantize_q8_1")
+
+
+def qmm_moe_gemv_q8(h, t, w_ptrs, scales, q, d, y, in_f, n_ff, n_used, t_tokens, stream=None) -> None:
+    _check(load().qmm_moe_gemv_q8(h, _dt(t), _ptr(w_ptrs), _ptr(scales), _ptr(q), _ptr(d), _ptr(y), in_f, n_ff,
+                                  n_used, t_tokens, _stream(stream)), "qmm_moe_gemv_q8")
+
+
+def qmm_moe_down_q8(h, t, w_ptrs, scales, q, d, y, n_ff, gin, n_used, t_tokens, workspace=None, workspace_bytes=None,
+                    stream=None) -> None:
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None or isinstance(workspace, int) else workspace.numel() * workspace.element_size()
+    _check(load().qmm_moe_down_q8(h, _dt(t), _ptr(w_ptrs), _ptr(scales), _ptr(q), _ptr(d), _ptr(y), n_ff, gin,
+                                  n_used, t_tokens, _ptr(workspace), workspace_bytes, _stream(stream)),
+           "qmm_moe_down_q8")
+
+
 def qmm_nvfp4_repack_v2(h, v1, v2, m, k, stream=None) -> None:
     _check(load().qmm_nvfp4_repack_v2(h, _ptr(v1), _ptr(v2), m, k, _stream(stream)), "qmm_nvfp4_repack_v2")
 
@@ -201,6 +229,12 @@ def qmm_gemm_noalloc(t, w, x, dst, m, k, n, stream=None) -> None:
     share it, so they must not overlap on the GPU)."""
     _check(load().qmm_gemm_noalloc(_dt(t), _ptr(w), _ptr(x), _ptr(dst), m, k, n, _stream(stream)),
            "qmm_gemm_noalloc")
+
+
+def qmm_gemm_noalloc_status(stream=None) -> int:
+    """Synchronize and return (and clear) the device status latched by
+    qmm_gemm_noalloc calls on the current device (0 = ok); never raises."""
+    return load().qmm_gemm_noalloc_status(_stream(stream))
 
 
 def qmm_testing_set_wait_limit_ns(h, limit_ns: int) -> None:

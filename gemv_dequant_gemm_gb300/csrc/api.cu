@@ -267,6 +267,82 @@ int qmm_moe_down(qmm_handle h, qmm_dtype t, const void *const *w_ptrs, const flo
     });
 }
 
+int qmm_quantize_q8_1(qmm_handle h, const float *x, int8_t *q, float *d, int64_t rows, int64_t k, void *stream) {
+    if (!valid_handle(h) || !x || !q || !d) return QMM_ERR_INVALID_ARG;
+    if (rows < 1 || rows > kMaxMN || k < 32 || k > kMaxK || k % 32 != 0) return QMM_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(d)) return QMM_ERR_ALIGN;
+    const size_t xbytes = static_cast<size_t>(rows * k) * sizeof(float);
+    const size_t qbytes = static_cast<size_t>(rows * k), dbytes = static_cast<size_t>(rows * (k / 32)) * sizeof(float);
+    if (overlaps(q, qbytes, x, xbytes) || overlaps(d, dbytes, x, xbytes) || overlaps(q, qbytes, d, dbytes))
+        return QMM_ERR_OVERLAP;
+    return on_device(h, [&] {
+        return qmm::launch_quantize_q8_1(x, q, d, rows, k, h->num_sms, static_cast<cudaStream_t>(stream));
+    });
+}
+
+int qmm_moe_gemv_q8(qmm_handle h, qmm_dtype t, const void *const *w_ptrs, const float *scales, const int8_t *q,
+                    const float *d, float *y, int64_t in_f, int64_t n_ff, int n_used, int t_tokens, void *stream) {
+    if (!valid_handle(h) || !known_dtype(t) || !w_ptrs || !scales || !q || !d || !y) return QMM_ERR_INVALID_ARG;
+    if (t != QMM_NVFP4 && t != QMM_NVFP4_V2) return QMM_ERR_UNSUPPORTED;
+    if (n_used < 1 || t_tokens < 1 || static_cast<int64_t>(n_used) * t_tokens > 4096) return QMM_ERR_SHAPE;
+    if (n_ff < 1 || n_ff > kMaxMN || in_f < 64 || in_f > QMM_Q8_MAX_K || in_f % 64 != 0) return QMM_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(w_ptrs) & 7u) != 0 || (reinterpret_cast<uintptr_t>(scales) & 3u) != 0 ||
+        !aligned16(q) || !aligned16(d) || !aligned16(y))
+        return QMM_ERR_ALIGN;
+    const int n_pairs = n_used * t_tokens;
+    const size_t ybytes = static_cast<size_t>(2) * n_pairs * n_ff * sizeof(float);
+    if (overlaps(y, ybytes, q, static_cast<size_t>(t_tokens) * in_f) ||
+        overlaps(y, ybytes, d, static_cast<size_t>(t_tokens) * (in_f / 32) * sizeof(float)) ||
+        overlaps(y, ybytes, scales, static_cast<size_t>(2) * n_pairs * sizeof(float)) ||
+        overlaps(y, ybytes, w_ptrs, static_cast<size_t>(2) * n_pairs * sizeof(void *)))
+        return QMM_ERR_OVERLAP;
+    const int64_t rb = qmm_row_bytes(t, in_f);
+    return on_device(h, [&] {
+        return qmm::launch_moe_q8(t, w_ptrs, rb, scales, q, d, y, in_f, n_ff, 2 * n_pairs, n_pairs, n_used,
+                                  h->num_sms, h->d_status, h->wait_limit_ns, static_cast<cudaStream_t>(stream));
+    });
+}
+
+int qmm_moe_down_q8(qmm_handle h, qmm_dtype t, const void *const *w_ptrs, const float *scales, const int8_t *q,
+                    const float *d, float *y, int64_t n_ff, int64_t gin, int n_used, int t_tokens, void *workspace,
+                    size_t workspace_bytes, void *stream) {
+    if (!valid_handle(h) || !known_dtype(t) || !w_ptrs || !scales || !q || !d || !y) return QMM_ERR_INVALID_ARG;
+    if (t != QMM_NVFP4 && t != QMM_NVFP4_V2) return QMM_ERR_UNSUPPORTED;
+    if (n_used < 1 || t_tokens < 1 || static_cast<int64_t>(n_used) * t_tokens > 4096) return QMM_ERR_SHAPE;
+    if (gin < 1 || gin > kMaxMN || n_ff < 64 || n_ff > QMM_Q8_MAX_K || n_ff % 64 != 0) return QMM_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(w_ptrs) & 7u) != 0 || (reinterpret_cast<uintptr_t>(scales) & 3u) != 0 ||
+        !aligned16(q) || !aligned16(d) || !aligned16(y))
+        return QMM_ERR_ALIGN;
+    const int n_pairs = n_used * t_tokens;
+    const size_t ybytes = static_cast<size_t>(t_tokens) * gin * sizeof(float);
+    const size_t qbytes = static_cast<size_t>(n_pairs) * n_ff;
+    const size_t dbytes = static_cast<size_t>(n_pairs) * (n_ff / 32) * sizeof(float);
+    const size_t sbytes = static_cast<size_t>(n_pairs) * sizeof(float);
+    const size_t pbytes = static_cast<size_t>(n_pairs) * sizeof(void *);
+    if (overlaps(y, ybytes, q, qbytes) || overlaps(y, ybytes, d, dbytes) || overlaps(y, ybytes, scales, sbytes) ||
+        overlaps(y, ybytes, w_ptrs, pbytes))
+        return QMM_ERR_OVERLAP;
+    const size_t need = qmm_moe_down_workspace_bytes(gin, n_used, t_tokens);
+    if (need) {
+        if (!workspace || workspace_bytes < need) return QMM_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return QMM_ERR_ALIGN;
+        if (overlaps(workspace, need, y, ybytes) || overlaps(workspace, need, q, qbytes) ||
+            overlaps(workspace, need, d, dbytes) || overlaps(workspace, need, scales, sbytes) ||
+            overlaps(workspace, need, w_ptrs, pbytes))
+            return QMM_ERR_OVERLAP;
+    }
+    const int64_t rb = qmm_row_bytes(t, n_ff);
+    return on_device(h, [&]() -> cudaError_t {
+        // the pair products (activation row = pair), then the per-token combine
+        float *part = n_used == 1 ? y : static_cast<float *>(workspace);
+        cudaError_t e = qmm::launch_moe_q8(t, w_ptrs, rb, scales, q, d, part, n_ff, gin, n_pairs, n_pairs, 1,
+                                           h->num_sms, h->d_status, h->wait_limit_ns,
+                                           static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess || n_used == 1) return e;
+        return qmm::launch_moe_combine(part, y, gin, n_used, t_tokens, h->num_sms, static_cast<cudaStream_t>(stream));
+    });
+}
+
 int qmm_dequant(qmm_handle h, qmm_dtype t, const void *w, float *out, int64_t m, int64_t k, float tensor_scale,
                 void *stream) {
     if (!valid_handle(h) || !known_dtype(t) || !w || !out) return QMM_ERR_INVALID_ARG;

@@ -52,6 +52,26 @@ __device__ __forceinline__ float e2m1_to_f32(uint32_t code) {
     return (code & 8u) ? -mag : mag;
 }
 
+// Four E2M1 codes (the low 16 bits of `sel`, one per nibble) -> four bytes
+// 2*value + 12 (0..24), by byte permutation only.  The positive table covers
+// codes 0..7; a code with its sign bit set makes the permute replicate the
+// (clear) top bit of its table byte, giving 0.  The negative table is indexed
+// with the sign bits flipped, so for every code one of the two lookups is 0
+// and the OR is the other.
+// (PTX prmt in its default mode: a selector nibble's top bit asks for the
+// sign of the chosen byte replicated; __byte_perm ignores that bit.)
+__device__ __forceinline__ uint32_t prmt_signed(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t e2m1x4_offset_bytes(uint32_t sel) {
+    const uint32_t pos = prmt_signed(0x0F0E0D0Cu, 0x18141210u, sel);           // 12 + 2*{0,.5,1,1.5,2,3,4,6}
+    const uint32_t neg = prmt_signed(0x090A0B0Cu, 0x00040608u, sel ^ 0x8888u);  // 12 - 2*{0,.5,1,1.5,2,3,4,6}
+    return pos | neg;
+}
+
 // Byte loaders: read-only global loads, or shared-memory loads through a
 // generic pointer into shared memory.  The decoders below are written once
 // against either.

@@ -204,26 +204,6 @@ template <> __device__ __forceinline__ void grp8<QMM_Q6_K>(const uint8_t *row, i
     }
 }
 
-// Four E2M1 codes (the low 16 bits of `sel`, one per nibble) -> four bytes
-// 2*value + 12 (0..24), by byte permutation only.  The positive table covers
-// codes 0..7; a code with its sign bit set makes the permute replicate the
-// (clear) top bit of its table byte, giving 0.  The negative table is indexed
-// with the sign bits flipped, so for every code one of the two lookups is 0
-// and the OR is the other.
-// (PTX prmt in its default mode: a selector nibble's top bit asks for the
-// sign of the chosen byte replicated; __byte_perm ignores that bit.)
-__device__ __forceinline__ uint32_t prmt_signed(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t d;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-    return d;
-}
-
-__device__ __forceinline__ uint32_t e2m1x4_offset_bytes(uint32_t sel) {
-    const uint32_t pos = prmt_signed(0x0F0E0D0Cu, 0x18141210u, sel);           // 12 + 2*{0,.5,1,1.5,2,3,4,6}
-    const uint32_t neg = prmt_signed(0x090A0B0Cu, 0x00040608u, sel ^ 0x8888u);  // 12 - 2*{0,.5,1,1.5,2,3,4,6}
-    return pos | neg;
-}
-
 template <> __device__ __forceinline__ void grp8<QMM_NVFP4>(const uint8_t *row, int64_t e0, int64_t, Grp &g) {
     const uint8_t *blk = row + (e0 >> 6) * 36;
     const int e = static_cast<int>(e0 & 63);
@@ -1181,11 +1161,16 @@ cudaError_t launch_moe_down(int dtype, const void *const *w_ptrs, int64_t rb, co
     plan_stages(p, static_cast<int64_t>(n_pairs) * n_ff * 4, gv::SMEM_BUDGET / 2);
     cudaError_t e = dispatch_any(dtype, rx_params(p), p, 1, num_sms, st);
     if (e != cudaSuccess || n_used == 1) return e;
+    return launch_moe_combine(part, y, gin, n_used, tokens, num_sms, st);
+}
+
+cudaError_t launch_moe_combine(const float *part, float *y, int64_t gin, int n_used, int tokens, int num_sms,
+                               cudaStream_t st) {
     const int64_t per = (gin & 3) == 0 ? gin / 4 : gin;
     const int64_t want = (tokens * per + 255) / 256;
     const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, 4LL * num_sms)));
-    return launch_pdl(moe_combine_kernel, dim3(grid), dim3(256), 0, st, dim3(1, 1, 1),
-                      static_cast<const float *>(part), y, gin, n_used, static_cast<int64_t>(tokens));
+    return launch_pdl(moe_combine_kernel, dim3(grid), dim3(256), 0, st, dim3(1, 1, 1), part, y, gin, n_used,
+                      static_cast<int64_t>(tokens));
 }
 
 }  // namespace qmm

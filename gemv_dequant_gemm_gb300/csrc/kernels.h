@@ -30,6 +30,22 @@ cudaError_t launch_moe_down(int dtype, const void *const *w_ptrs, int64_t rb, co
                             float *y, float *part, int64_t n_ff, int64_t gin, int n_used, int tokens, int num_sms,
                             uint32_t *status, uint64_t limit_ns, cudaStream_t st);
 
+// y[t][gin] = the fixed-order sum (u = 0, 1, ...) of part[t*n_used + u][gin].
+cudaError_t launch_moe_combine(const float *part, float *y, int64_t gin, int n_used, int tokens, int num_sms,
+                               cudaStream_t st);
+
+// Q8_1 activation blocks: q[rows][k] int8, d[rows][k/32] (k % 32 == 0).
+cudaError_t launch_quantize_q8_1(const float *x, int8_t *q, float *d, int64_t rows, int64_t k, int num_sms,
+                                 cudaStream_t st);
+
+// NVFP4 (36-byte groups or V2 rows) MoE products on Q8_1 activations:
+// dst[mat][r] = scales[mat] * sum_c W_mat[r][c] * q[a][c] * d[a][c/32] with
+// activation row a = (mat % n_pairs) / n_used, for mats matrices of
+// rows_per_mat rows; k % 64 == 0, k <= QMM_Q8_MAX_K.
+cudaError_t launch_moe_q8(int dtype, const void *const *w_ptrs, int64_t rb, const float *scales, const int8_t *q,
+                          const float *d, float *dst, int64_t k, int64_t rows_per_mat, int mats, int n_pairs,
+                          int n_used, int num_sms, uint32_t *status, uint64_t limit_ns, cudaStream_t st);
+
 // NVFP4 36-byte-group rows -> V2 rows (codes, then the scale stream); k % 64 == 0.
 cudaError_t launch_nvfp4_repack_v2(const uint8_t *v1, uint8_t *v2, int64_t m, int64_t k, int num_sms,
                                    cudaStream_t st);

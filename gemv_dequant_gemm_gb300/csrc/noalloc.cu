@@ -1,10 +1,13 @@
 // noalloc.cu -- qmm_gemm_noalloc: qmm_gemm without any device allocation, for
-// callers that cannot call cudaMalloc (see include/qmm.h).  The tensor-core
-// kernel's scratch (the f16 copy of X and a status word) lives in one
-// file-scope static device array; the existing launchers do the work.
+// callers that cannot call cudaMalloc (see include/qmm.h), and
+// qmm_gemm_noalloc_status, which reads the device status those calls latch.
+// The tensor-core kernel's scratch (the f16 copy of X and a status word)
+// lives in one file-scope static device array; the existing launchers do the
+// work.
 #include <mutex>
 
 #include "../../include/qmm.h"
+#include "common.cuh"
 #include "kernels.h"
 
 namespace {
@@ -20,8 +23,7 @@ constexpr int64_t kMaxK = int64_t(1) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratch];
 
 struct DeviceSetup {
-    bool ready;
-    int status;  // QMM_OK or the set-up failure
+    bool ready;  // set only once every step below has succeeded
     int num_sms;
     unsigned char *scratch;
 };
@@ -29,30 +31,31 @@ DeviceSetup g_setup[kMaxDevices];
 std::mutex g_setup_mu;
 
 // Set-up of the current device (with that device current): architecture check,
-// kernel attributes, and the device address of the static scratch array.
+// kernel attributes, and the device address of the static scratch array.  A
+// failure leaves the device not set up, so a later call tries again.  (The
+// array itself is zero when its module is placed on the device, so the status
+// word starts cleared.)
 int setup_current_device(int dev, DeviceSetup **out) {
     if (dev < 0 || dev >= kMaxDevices) return QMM_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_setup_mu);
     DeviceSetup &s = g_setup[dev];
     if (!s.ready) {
-        s.ready = true;
-        s.status = QMM_OK;
-        int major = 0, minor = 0;
+        int major = 0, minor = 0, sms = 0;
+        unsigned char *p = nullptr;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-            s.status = QMM_ERR_CUDA;
-        } else if (major != 10 || minor != 3) {
-            s.status = QMM_ERR_ARCH;
-        } else if (cudaGetSymbolAddress(reinterpret_cast<void **>(&s.scratch), g_noalloc_scratch) != cudaSuccess ||
-                   s.scratch == nullptr) {
-            s.status = QMM_ERR_CUDA;
-        } else if (qmm::gemm_tc_init() != cudaSuccess) {
-            s.status = QMM_ERR_CUDA;
-        }
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return QMM_ERR_CUDA;
+        if (major != 10 || minor != 3) return QMM_ERR_ARCH;
+        if (cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_noalloc_scratch) != cudaSuccess || p == nullptr)
+            return QMM_ERR_CUDA;
+        if (qmm::gemm_tc_init() != cudaSuccess) return QMM_ERR_CUDA;
+        s.num_sms = sms;
+        s.scratch = p;
+        s.ready = true;
     }
     *out = &s;
-    return s.status;
+    return QMM_OK;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -88,9 +91,10 @@ extern "C" int qmm_gemm_noalloc(qmm_dtype t, const void *w, const float *x, floa
     if (st != QMM_OK) return st;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
 
+    // device-side timeouts are OR-ed into the status word until
+    // qmm_gemm_noalloc_status reads and clears it
     uint32_t *status = reinterpret_cast<uint32_t *>(s->scratch);
-    cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), cs);  // the status word starts each call cleared
-    if (e != cudaSuccess) return QMM_ERR_CUDA;
+    cudaError_t e;
     if (!tensor_core) {
         e = qmm::launch_gemv(t, w, rb, x, dst, m, k, static_cast<int>(n), s->num_sms, status, 2000000000ull, cs);
     } else {
@@ -110,4 +114,24 @@ extern "C" int qmm_gemm_noalloc(qmm_dtype t, const void *w, const float *x, floa
         e = qmm::launch_gemm_tc(a, s->num_sms, cs);
     }
     return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
+}
+
+extern "C" int qmm_gemm_noalloc_status(void *stream) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return QMM_ERR_CUDA;
+    DeviceSetup *s = nullptr;
+    const int st = setup_current_device(dev, &s);
+    if (st != QMM_OK) return st;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    uint32_t bits = 0;  // host stack: no allocation on either side
+    if (cudaStreamSynchronize(cs) != cudaSuccess) return QMM_ERR_CUDA;
+    if (cudaMemcpy(&bits, s->scratch, sizeof(bits), cudaMemcpyDeviceToHost) != cudaSuccess) return QMM_ERR_CUDA;
+    if (bits != 0) {
+        if (cudaMemsetAsync(s->scratch, 0, sizeof(uint32_t), cs) != cudaSuccess ||
+            cudaStreamSynchronize(cs) != cudaSuccess)
+            return QMM_ERR_CUDA;
+    }
+    if (bits & qmm::kDevTimeout) return QMM_ERR_TIMEOUT;
+    if (bits & qmm::kDevBadPtr) return QMM_ERR_ALIGN;
+    return QMM_OK;
 }

@@ -209,6 +209,54 @@ int qmm_moe_down(qmm_handle h, qmm_dtype t, const void *const *w_ptrs, const flo
                  const float *hact, float *y, int64_t n_ff, int64_t gin, int n_used, int t_tokens,
                  void *workspace, size_t workspace_bytes, void *stream);
 
+/* Largest row length (in_f of qmm_moe_gemv_q8, n_ff of qmm_moe_down_q8) the
+ * int8-activation calls accept. */
+#define QMM_Q8_MAX_K 8192
+
+/* Q8_1 activation blocks (memra-engine 0.128.0
+ * src/bin/moe_rows_ceiling_bench.rs, main: quantize_q8_1 turns the f32
+ * activation into int8 codes with per-block scales before its served gate/up
+ * kernel; the page prints neither its code nor its rule).  For every block of
+ * 32 consecutive values of a row of x ([rows][k] float32, k % 32 == 0):
+ *   d = amax / 127,  q = x * (1/d) rounded to the nearest integer, halves away
+ *   from zero (q = 0 when d == 0),
+ * each step one float32 operation, so the integer codes are decided in
+ * float32 and match any IEEE float32 implementation of the same steps bit for
+ * bit.  q is [rows][k] int8, d is [rows][k/32] float32.  Device pointers, all
+ * 16-byte aligned, outputs overlapping no input; 1 <= rows <= 2^24, 32 <= k <=
+ * 2^20.  Errors: QMM_ERR_INVALID_ARG, QMM_ERR_SHAPE, QMM_ERR_ALIGN,
+ * QMM_ERR_OVERLAP, QMM_ERR_CUDA. */
+int qmm_quantize_q8_1(qmm_handle h, const float *x, int8_t *q, float *d, int64_t rows, int64_t k,
+                      void *stream);
+
+/* qmm_moe_gemv on Q8_1 activations (the same page's served gate/up kernel
+ * reads the quantized activation and names its PRMT/dp4a instruction stream):
+ *   y[p][j][r] = scales[p*n_pairs + j] * sum_c W_pj[r][c] * q[i][c] * d[i][c/32]
+ * with i = j / n_used, the token of pair j; q [t_tokens][in_f] int8 and d
+ * [t_tokens][in_f/32] float32 as qmm_quantize_q8_1 writes them.  NVFP4 and
+ * NVFP4_V2 weights only (QMM_ERR_UNSUPPORTED otherwise): each 16-weight
+ * region's product is an exact int32 dot product of 2*e2m1 codes and q,
+ * scaled once by its E4M3 scale and block scale d.  Accuracy |y - exact| <=
+ * 1e-5 * |scale| * sum_c |W * q*d| against the exact product on the quantized
+ * activation.  in_f % 64 == 0, in_f <= QMM_Q8_MAX_K; other sizes, pointer
+ * table, scales and y as qmm_moe_gemv; q, d 16-byte aligned.  The 7.0
+ * argument of the page's kernel (its meaning is not printed) is not applied.
+ * Errors as qmm_moe_gemv. */
+int qmm_moe_gemv_q8(qmm_handle h, qmm_dtype t, const void *const *w_ptrs, const float *scales,
+                    const int8_t *q, const float *d, float *y, int64_t in_f, int64_t n_ff, int n_used,
+                    int t_tokens, void *stream);
+
+/* qmm_moe_down on Q8_1 activations: hact[j][c] is given as q[j][c] *
+ * d[j][c/32] (q [n_pairs][n_ff] int8, d [n_pairs][n_ff/32] float32).  The
+ * same products, workspace and fixed-order combine as qmm_moe_down, with the
+ * arithmetic of qmm_moe_gemv_q8; NVFP4 and NVFP4_V2 only; n_ff % 64 == 0,
+ * n_ff <= QMM_Q8_MAX_K.  Accuracy |y - exact| <= 1e-5 * sum_u |scales[j]| *
+ * sum_c |W_j * q*d|.  Workspace: qmm_moe_down_workspace_bytes(gin, n_used,
+ * t_tokens).  Errors as qmm_moe_down. */
+int qmm_moe_down_q8(qmm_handle h, qmm_dtype t, const void *const *w_ptrs, const float *scales,
+                    const int8_t *q, const float *d, float *y, int64_t n_ff, int64_t gin, int n_used,
+                    int t_tokens, void *workspace, size_t workspace_bytes, void *stream);
+
 /* Repack NVFP4 rows into the V2 layout (memra-engine 0.128.0
  * src/bin/moe_rows_ceiling_bench.rs, main: the V2 arms read the same values
  * through rows repacked with the scales split out).  v1 is [m] rows of
@@ -249,26 +297,46 @@ int qmm_sync_status(qmm_handle h, void *stream);
  * start-up).  It needs neither a handle (qmm_create allocates a status word)
  * nor a caller workspace: the f16 copy of X that the tensor-core kernel reads
  * lives in a static device array of QMM_NOALLOC_SCRATCH_BYTES built into the
- * library, which every GPU that loads the library holds until the process
- * exits.  The paper pages have no counterpart of this call.
+ * library.  The paper pages have no counterpart of this call.
  *   - Same product, layouts, accuracy and size rules as qmm_gemm, on the
  *     current device; n <= QMM_GEMV_MAX_N goes to the GEMV kernel as there.
  *   - n * k * 2 must not exceed QMM_NOALLOC_SCRATCH_BYTES - 256 when
  *     n > QMM_GEMV_MAX_N and the weights are packed; larger problems return
  *     QMM_ERR_WORKSPACE.
- *   - The first call on a device sets that device up (looks up the scratch
+ *   - When the memory is taken: under CUDA's lazy module loading (the
+ *     default, CUDA_MODULE_LOADING=LAZY) the driver places the scratch array
+ *     and each kernel on a device the first time they are used there, not
+ *     when the library is loaded.  So the first call on a device (of this
+ *     function or of qmm_gemm_noalloc_status) takes the array's memory, and
+ *     the first call that runs a given kernel (tensor-core or GEMV path, per
+ *     dtype) loads that kernel's code.  Callers that cannot allocate later
+ *     should make those calls at start-up, or set CUDA_MODULE_LOADING=EAGER
+ *     before CUDA initializes, which places everything when the context is
+ *     created.  After that, calls allocate nothing.
+ *   - The first call on a device also sets that device up (looks up the
  *     array's device address, checks the architecture, sets kernel
- *     attributes); make that first call before any stream capture.
+ *     attributes); make it before any stream capture.  A set-up that fails
+ *     is retried by the next call.
  *   - Every call shares the one scratch array, whose contents persist from
  *     call to call: calls that overlap on the GPU (on different streams, or
  *     from different threads) race on it.  Serialize them.
  *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library
- *     routine.  Device-side wait timeouts are latched in the scratch area but
- *     not reported (there is no handle to report them through).
+ *     routine.  Device-side wait timeouts are latched in the scratch array's
+ *     status word; read them with qmm_gemm_noalloc_status.
  * Errors: QMM_ERR_INVALID_ARG, QMM_ERR_SHAPE, QMM_ERR_ALIGN,
- * QMM_ERR_OVERLAP, QMM_ERR_WORKSPACE, QMM_ERR_ARCH, QMM_ERR_CUDA. */
+ * QMM_ERR_OVERLAP, QMM_ERR_WORKSPACE, QMM_ERR_UNSUPPORTED, QMM_ERR_ARCH,
+ * QMM_ERR_CUDA. */
 int qmm_gemm_noalloc(qmm_dtype t, const void *w, const float *x, float *dst, int64_t m, int64_t k,
                      int64_t n, void *stream);
+
+/* The device status latched by qmm_gemm_noalloc calls on the current device
+ * since the last read: synchronizes `stream`, copies the status word into a
+ * host variable, clears it and returns QMM_OK, QMM_ERR_TIMEOUT (a bounded
+ * wait ran out; the output of a call since the last read is not valid) or
+ * QMM_ERR_CUDA.  Allocates nothing.  It sets the device up like the first
+ * qmm_gemm_noalloc call, so a caller can also use it at start-up for that.
+ * The paper pages have no counterpart of this call. */
+int qmm_gemm_noalloc_status(void *stream);
 
 #ifdef __cplusplus
 }

@@ -79,3 +79,4 @@ def test_null_handle_and_arguments_are_rejected_without_a_device():
 def test_create_fails_loudly_without_a_gpu():
     with pytest.raises(q.QmmError):
         q.qmm_create(0)
+    assert q.load().qmm_gemm_noalloc_status(None) == 6  # QMM_ERR_CUDA: no device to set up

@@ -108,8 +108,11 @@ def _exact_weights(fmt, m, k, rng):
     if fmt == "q4_k":
         blk = rng.integers(0, 256, (m * nb, 144)).astype(np.uint8)
         blk[:, 0:4] = [0x00, 0x38, 0x00, 0x34]  # d = 0.5, dmin = 0.25
-        blk[:, 4:12] &= 0x1F  # 6-bit fields of sub-blocks 0..3 at most 31, high bits of 4..7 zero
-        blk[:, 12:16] &= 0xFF  # low nibbles of sub-blocks 4..7: at most 15
+        # every 6-bit scale and minimum at most 15 (fields of sub-blocks 0..3
+        # below 16, the high bits of sub-blocks 4..7 zero, their low nibbles
+        # as drawn): |W| <= 0.5*15*15, so sums over k = 4608 of products with
+        # X (multiples of 1/8) stay exact in f32
+        blk[:, 4:12] &= 0x0F
         return blk.reshape(-1)
     if fmt == "q6_k":
         blk = rng.integers(0, 256, (m * nb, 210)).astype(np.uint8)
@@ -135,16 +138,39 @@ def test_exact_arithmetic_is_bit_identical(h, fmt, m, k, n):
     assert_bitexact(got, ref.astype(np.float32), f"{fmt} {m}x{k}x{n}")
 
 
-@pytest.mark.parametrize("fmt", ["f32", "q4_0", "q8_0"])
-def test_exact_arithmetic_full_prefill_shape(h, fmt):
-    m, k, n = 4608, 1024, 512
+# Full-size exact-arithmetic cases, every output element compared bit for
+# bit with the oracle: ffn_gate at n = 512 (one 128-row tile per CTA, no
+# split-K), ffn_down at n = 512 (split-K over a cluster of four), and
+# 4864 x 512 x 1024, where 38 row tiles x 8 token tiles exceed the 152 SMs
+# while 19 two-subtile CTAs x 8 cover them exactly: the launcher takes the
+# two-subtile (256-row) CTAs there.
+FULL_EXACT = {"ffn_gate": (4608, 1024, 512), "ffn_down": (1024, 4608, 512), "two_subtiles": (4864, 512, 1024)}
+
+
+@pytest.mark.parametrize("case", list(FULL_EXACT))
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_exact_arithmetic_full_size_every_element(h, fmt, case):
+    m, k, n = FULL_EXACT[case]
+    if fmt == "f32" and case == "two_subtiles":
+        pytest.skip("f32 weights have no two-subtile variant")
     rng = np.random.default_rng(23)
     w = _exact_weights(fmt, m, k, rng)
     x = (rng.integers(-8, 9, (n, k)) / 8).astype(np.float32)
+    ref, _ = oracle.matmul(fmt, w, x, m, k, n)
+    assert np.array_equal(ref, ref.astype(np.float32).astype(np.float64)), "case is not exact in f32"
     got = _gemm(h, fmt, w, x, m, k, n).cpu().numpy()
-    ni, mj = tile_samples(m, n, per_tile=8)
-    ref, _ = oracle.matmul_entries(fmt, w, x, m, k, n, ni, mj)
-    assert_bitexact(got[ni, mj], ref.astype(np.float32), fmt)
+    assert_bitexact(got, ref.astype(np.float32), f"{fmt} {case} {m}x{k}x{n}")
+
+
+@pytest.mark.parametrize("fmt", ["q4_k", "q6_k", "nvfp4"])
+def test_prefill_ffn_down_every_element(h, fmt):
+    # the split-K path on random packed bytes, every element within tolerance
+    m, k = LFM2_SHAPES["ffn_down"]
+    n = 512
+    w, x = weights(fmt, m, k), synth.activations(n, k)
+    ref, am = oracle.matmul(fmt, w, x, m, k, n)
+    got = _gemm(h, fmt, w, x, m, k, n).cpu().numpy()
+    assert_close(got, ref, am, TC_REL, TC_ABS, what=f"{fmt} ffn_down")
 
 
 def test_gemm_is_deterministic(h):

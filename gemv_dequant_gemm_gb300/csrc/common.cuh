@@ -285,6 +285,59 @@ __host__ __device__ constexpr uint32_t mma_idesc(uint32_t ab_format, uint32_t m,
            | ((m >> 4) << 24);     // M / 16
 }
 
+// ---- thread-block clusters ----------------------------------------------------
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+// (no memory clobber: the partials were published by the cluster barrier
+// before the first of these loads and are not written again until the next one)
+__device__ __forceinline__ float4 ld_dsmem_v4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ int ld_dsmem_u32(uint32_t addr) {
+    int v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// Butterfly reduction of V values (a power of two <= 32) over the warp:
+// afterwards lane l holds the warp total of value l % V in a[0].
+template <int V> __device__ __forceinline__ float warp_transpose_sum(float (&a)[V], int lane) {
+#pragma unroll
+    for (int h = V / 2; h >= 1; h >>= 1) {
+        const bool upper = (lane & h) != 0;
+#pragma unroll
+        for (int t = 0; t < h; ++t) {
+            const float send = upper ? a[t] : a[t + h];
+            const float keep = upper ? a[t + h] : a[t];
+            a[t] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, h);
+        }
+    }
+#pragma unroll
+    for (int off = V; off < 32; off <<= 1) a[0] += __shfl_xor_sync(0xFFFFFFFFu, a[0], off);
+    return a[0];
+}
+
 // Launch `kernel` on `st` with programmatic dependent launch allowed (and an
 // optional cluster shape; 1 x 1 x 1 launches without clusters).
 template <typename... KArgs, typename... Args>

@@ -100,139 +100,6 @@ __device__ __forceinline__ bool mbar_wait_drain_any(uint64_t *bar, uint32_t pari
     }
 }
 
-// ---------------------------------------------------------------------------
-// Group decoders for the dot products: 8 weights of one scale region as small
-// exact values v[j] plus the region's scale, so that
-//     sum_j W_j x_j = scale * sum_j v_j x_j            (Q4_0, Q8_0, Q6_K, NVFP4)
-//     sum_j W_j x_j = a * sum_j q_j x_j - b * sum_j x_j (Q4_K: W = a q - b)
-// The integer-valued codes become floats by placing them under the exponent of
-// 2^23 and subtracting 2^23 (plus the code's bias), all exact and all on the
-// integer and FMA pipes (no conversion instructions).
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ float byte_as_float(uint32_t word, int j, float minus) {
-    return __uint_as_float(__byte_perm(word, 0x4B000000u, 0x7440u | static_cast<uint32_t>(j))) - minus;
-}
-
-struct Grp {
-    float v[8];
-    float scale;   // multiplies sum v x
-    float offset;  // Q4_K: b, subtracted as b * sum x (0 otherwise)
-};
-
-template <int F> __device__ __forceinline__ void grp8(const uint8_t *row, int64_t e0, int64_t k, Grp &g);
-
-template <> __device__ __forceinline__ void grp8<QMM_F32>(const uint8_t *row, int64_t e0, int64_t k, Grp &g) {
-    decode8_f32<LdS>(row, e0, k, g.v);
-    g.scale = 1.0f;
-    g.offset = 0.0f;
-}
-
-template <> __device__ __forceinline__ void grp8<QMM_Q4_0>(const uint8_t *row, int64_t e0, int64_t, Grp &g) {
-    const uint8_t *blk = row + (e0 >> 5) * 18;
-    const int e = static_cast<int>(e0 & 31);
-    g.scale = half_bits_to_f32(LdS::u16(blk));
-    g.offset = 0.0f;
-    const uint8_t *q = blk + 2 + (e & 15);
-    uint32_t lo = ld_u32_a2<LdS>(q), hi = ld_u32_a2<LdS>(q + 4);
-    if (e >= 16) {
-        lo >>= 4;
-        hi >>= 4;
-    }
-    lo &= 0x0F0F0F0Fu;
-    hi &= 0x0F0F0F0Fu;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        g.v[j] = byte_as_float(lo, j, 8388616.0f);  // q - 8
-        g.v[4 + j] = byte_as_float(hi, j, 8388616.0f);
-    }
-}
-
-template <> __device__ __forceinline__ void grp8<QMM_Q8_0>(const uint8_t *row, int64_t e0, int64_t, Grp &g) {
-    const uint8_t *blk = row + (e0 >> 5) * 34;
-    const int e = static_cast<int>(e0 & 31);
-    g.scale = half_bits_to_f32(LdS::u16(blk));
-    g.offset = 0.0f;
-    const uint8_t *q = blk + 2 + e;
-    const uint32_t lo = ld_u32_a2<LdS>(q) ^ 0x80808080u, hi = ld_u32_a2<LdS>(q + 4) ^ 0x80808080u;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        g.v[j] = byte_as_float(lo, j, 8388736.0f);  // (q + 128) - 128
-        g.v[4 + j] = byte_as_float(hi, j, 8388736.0f);
-    }
-}
-
-template <> __device__ __forceinline__ void grp8<QMM_Q4_K>(const uint8_t *row, int64_t e0, int64_t, Grp &g) {
-    const uint8_t *blk = row + (e0 >> 8) * 144;
-    const int e = static_cast<int>(e0 & 255);
-    const uint32_t dd = LdS::u32(blk);
-    int sc, mn;
-    q4k_sc_min<LdS>(blk + 4, e >> 5, sc, mn);
-    g.scale = __fmul_rn(half_bits_to_f32(dd & 0xFFFFu), static_cast<float>(sc));
-    g.offset = __fmul_rn(half_bits_to_f32(dd >> 16), static_cast<float>(mn));
-    const int c = e >> 6, r = e & 63;
-    uint2 q = LdS::u64(blk + 16 + 32 * c + (r & 31));
-    if (r >= 32) {
-        q.x >>= 4;
-        q.y >>= 4;
-    }
-    q.x &= 0x0F0F0F0Fu;
-    q.y &= 0x0F0F0F0Fu;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        g.v[j] = byte_as_float(q.x, j, 8388608.0f);
-        g.v[4 + j] = byte_as_float(q.y, j, 8388608.0f);
-    }
-}
-
-template <> __device__ __forceinline__ void grp8<QMM_Q6_K>(const uint8_t *row, int64_t e0, int64_t, Grp &g) {
-    const uint8_t *blk = row + (e0 >> 8) * 210;
-    const int e = static_cast<int>(e0 & 255);
-    const int h = e >> 7, rr = e & 127, s = rr >> 5, l = rr & 31;
-    const float d = half_bits_to_f32(LdS::u16(blk + 208));
-    g.scale = __fmul_rn(d, static_cast<float>(static_cast<int8_t>(LdS::u8(blk + 192 + 8 * h + (l >> 4) + 2 * s))));
-    g.offset = 0.0f;
-    const uint8_t *ql = blk + 64 * h + l + 32 * (s & 1);
-    const uint8_t *qh = blk + 128 + 32 * h + l;
-    const int lsh = (s >= 2) ? 4 : 0, hsh = 2 * s;
-    const uint32_t q0 = ((ld_u32_a2<LdS>(ql) >> lsh) & 0x0F0F0F0Fu) | (((ld_u32_a2<LdS>(qh) >> hsh) & 0x03030303u) << 4);
-    const uint32_t q1 =
-        ((ld_u32_a2<LdS>(ql + 4) >> lsh) & 0x0F0F0F0Fu) | (((ld_u32_a2<LdS>(qh + 4) >> hsh) & 0x03030303u) << 4);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        g.v[j] = byte_as_float(q0, j, 8388640.0f);  // q - 32
-        g.v[4 + j] = byte_as_float(q1, j, 8388640.0f);
-    }
-}
-
-template <> __device__ __forceinline__ void grp8<QMM_NVFP4>(const uint8_t *row, int64_t e0, int64_t, Grp &g) {
-    const uint8_t *blk = row + (e0 >> 6) * 36;
-    const int e = static_cast<int>(e0 & 63);
-    g.scale = 0.5f * e4m3_to_f32(LdS::u8(blk + (e >> 4)));  // the bytes below hold 2 * value
-    g.offset = 0.0f;
-    const uint32_t codes = LdS::u32(blk + 4 + (e >> 1));
-    const uint32_t lo = e2m1x4_offset_bytes(codes & 0xFFFFu), hi = e2m1x4_offset_bytes(codes >> 16);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        g.v[j] = byte_as_float(lo, j, 8388620.0f);  // (2v + 12) - 12
-        g.v[4 + j] = byte_as_float(hi, j, 8388620.0f);
-    }
-}
-
-// NVFP4 V2 row (k/2 code bytes, then k/16 E4M3 scale bytes): the same
-// decode as the 36-byte groups, with the codes at e0/2 and the scale at
-// k/2 + e0/16 (k % 64 == 0 keeps the code word 4-byte aligned).
-template <> __device__ __forceinline__ void grp8<QMM_NVFP4_V2>(const uint8_t *row, int64_t e0, int64_t k, Grp &g) {
-    g.scale = 0.5f * e4m3_to_f32(LdS::u8(row + (k >> 1) + (e0 >> 4)));  // the bytes below hold 2 * value
-    g.offset = 0.0f;
-    const uint32_t codes = LdS::u32(row + (e0 >> 1));
-    const uint32_t lo = e2m1x4_offset_bytes(codes & 0xFFFFu), hi = e2m1x4_offset_bytes(codes >> 16);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        g.v[j] = byte_as_float(lo, j, 8388620.0f);  // (2v + 12) - 12
-        g.v[4 + j] = byte_as_float(hi, j, 8388620.0f);
-    }
-}
-
 // 8 consecutive X values of one activation row (shared or global memory).
 __device__ __forceinline__ void load_x8(const float *xr, bool in_smem, int64_t e0, int64_t k, float (&v)[8]) {
     if (e0 + 8 <= k && (k % 4) == 0) {
@@ -558,67 +425,6 @@ template <> struct UnitDec<QMM_NVFP4, 16> {
     }
 };
 
-// Packed pairs of f32 (Blackwell f32x2 arithmetic: two independent
-// round-to-nearest operations per instruction, same results as scalar ones).
-__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ float2 f2_unpack(uint64_t v) {
-    float2 r;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
-    return r;
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint32_t lds8(uint32_t a) {
-    uint16_t v;
-    asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(a));
-    return v;
-}
-__device__ __forceinline__ uint32_t lds32(uint32_t a) {
-    uint32_t v;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
-    return v;
-}
-
-// Two E2M1 codes of one byte as an exact f32 pair (element of the low nibble
-// first): the hardware E2M1 -> f16x2 conversion, then f16 -> f32 widening,
-// both exact for every code.
-__device__ __forceinline__ uint64_t f16x2_to_f2(uint32_t h) {
-    uint64_t r;
-    asm("{\n\t.reg .b16 lo, hi;\n\t.reg .f32 a, b;\n\t"
-        "mov.b32 {lo, hi}, %1;\n\t"
-        "cvt.f32.f16 a, lo;\n\t"
-        "cvt.f32.f16 b, hi;\n\t"
-        "mov.b64 %0, {a, b};\n\t}"
-        : "=l"(r) : "r"(h));
-    return r;
-}
-__device__ __forceinline__ void e2m1x8_to_f2(uint32_t c, uint64_t *w) {
-    uint32_t h0, h1, h2, h3;
-    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-        : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3) : "r"(c));
-    w[0] = f16x2_to_f2(h0);
-    w[1] = f16x2_to_f2(h1);
-    w[2] = f16x2_to_f2(h2);
-    w[3] = f16x2_to_f2(h3);
-}
-
 // 16 NVFP4 weights of one scale region (codes at shared address `codes`,
 // scale byte at `scb`) as 8 exact f32 pairs of their E2M1 values; *scale
 // receives the e4m3 scale.
@@ -657,24 +463,6 @@ template <int UW> __device__ __forceinline__ void load_xu(const float *xr, int64
 #pragma unroll
         for (int j = 0; j < UW; ++j) v[j] = (e0 + j < k) ? __ldg(xr + e0 + j) : 0.0f;
     }
-}
-
-// Butterfly reduction of V values (a power of two <= 32) over the warp:
-// afterwards lane l holds the warp total of value l % V in a[0].
-template <int V> __device__ __forceinline__ float warp_transpose_sum(float (&a)[V], int lane) {
-#pragma unroll
-    for (int h = V / 2; h >= 1; h >>= 1) {
-        const bool upper = (lane & h) != 0;
-#pragma unroll
-        for (int t = 0; t < h; ++t) {
-            const float send = upper ? a[t] : a[t + h];
-            const float keep = upper ? a[t + h] : a[t];
-            a[t] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, h);
-        }
-    }
-#pragma unroll
-    for (int off = V; off < 32; off <<= 1) a[0] += __shfl_xor_sync(0xFFFFFFFFu, a[0], off);
-    return a[0];
 }
 
 template <int F, int NV, int JM>
@@ -1065,6 +853,11 @@ static gr::Params rx_params(const gv::Params &g) {
 
 cudaError_t launch_gemv(int dtype, const void *w, int64_t rb, const float *x, float *dst, int64_t m, int64_t k, int n,
                         int num_sms, uint32_t *status, uint64_t limit_ns, cudaStream_t st) {
+    // the split-K register-X kernel first (short calls: many small CTAs); if
+    // it has no plan, or its launch is refused, the kernels below run
+    const cudaError_t es = launch_gemv_sk(dtype, w, rb, x, dst, m, k, n, num_sms, status, limit_ns, st);
+    if (es == cudaSuccess) return es;
+    if (es != cudaErrorNotSupported) (void)cudaGetLastError();
     gv::Params p = {};
     p.w = static_cast<const uint8_t *>(w);
     p.x = x;

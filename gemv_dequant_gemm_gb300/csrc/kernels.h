@@ -18,6 +18,11 @@ cudaError_t launch_dequant(int dtype, const void *w, float *out, int64_t m, int6
 cudaError_t launch_gemv(int dtype, const void *w, int64_t rb, const float *x, float *dst, int64_t m, int64_t k,
                         int n, int num_sms, uint32_t *status, uint64_t limit_ns, cudaStream_t st);
 
+// The split-K register-X GEMV for Q4_0/Q8_0/Q4_K/Q6_K/NVFP4 when it has a plan
+// for the problem; cudaErrorNotSupported (nothing launched) otherwise.
+cudaError_t launch_gemv_sk(int dtype, const void *w, int64_t rb, const float *x, float *dst, int64_t m, int64_t k,
+                           int n, int num_sms, uint32_t *status, uint64_t limit_ns, cudaStream_t st);
+
 // MoE gate/up GEMV over 2 * n_pairs matrices; tokens = rows of x.
 cudaError_t launch_moe_gemv(int dtype, const void *const *w_ptrs, int64_t rb, const float *scales, const float *x,
                             float *y, int64_t in_f, int64_t n_ff, int n_used, int n_pairs, int tokens, int num_sms,

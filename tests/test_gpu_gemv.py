@@ -36,6 +36,17 @@ def test_gemv_decode_workload(h, fmt, m, k, n):
     assert_close(_gemv(h, fmt, w, x, m, k, n), ref, am, FMA_REL, what=f"{fmt} {m}x{k} n={n}")
 
 
+# shapes whose plans split k over clusters of 1 to 8 CTAs, with a ragged last
+# row block, and every n class of the register layout
+@pytest.mark.parametrize("n", [1, 3, 5, 8])
+@pytest.mark.parametrize("fmt,m,k", [("q6_k", 1001, 4608), ("q4_0", 333, 6144), ("nvfp4", 517, 2560),
+                                     ("q8_0", 2050, 1536), ("q4_k", 97, 9216), ("q8_0", 5, 512)])
+def test_gemv_split_k_plans(h, fmt, m, k, n):
+    w, x = weights(fmt, m, k), synth.activations(n, k)
+    ref, am = oracle.matmul(fmt, w, x, m, k, n)
+    assert_close(_gemv(h, fmt, w, x, m, k, n), ref, am, FMA_REL, what=f"{fmt} {m}x{k} n={n}")
+
+
 @pytest.mark.parametrize("fmt", ["q4_0", "q6_k", "nvfp4", "f32"])
 def test_gemv_other_formats_full_shape(h, fmt):
     m, k, n = 1024, 4608, 3

@@ -40,6 +40,11 @@ def test_dequant_v2_bit_exact(h, ts):
     assert np.array_equal(want, oracle.dequant("nvfp4", v1, m, k, ts))
 
 
+# The plain GEMV reads 36-byte-group rows through the split-K kernel and V2
+# rows through the shared-memory X / register-X kernels, whose summation
+# orders differ: both are held to the oracle's tolerance and to each other's
+# within it (the MoE calls below, one kernel for both layouts, stay
+# bit-identical).
 @pytest.mark.parametrize("m,k", [(300, 512), (1024, 4096)])  # shared-memory X kernel, register-X kernel
 def test_gemv_v2_matches_oracle_and_v1(h, m, k):
     v1, v2 = _v1_v2(m, k, 0x7201 + k)
@@ -52,9 +57,10 @@ def test_gemv_v2_matches_oracle_and_v1(h, m, k):
         q.qmm_gemv(h, "nvfp4_v2", d2, xd, y2, m, k, n)
         assert q.qmm_sync_status(h) == 0
         ref, am = oracle.matmul("nvfp4_v2", v2, x, m, k, n)
-        g2 = y2.cpu().numpy()
-        assert_close(g2, ref, am, FMA_REL, what=f"n={n}")
-        assert np.array_equal(g2.view(np.uint32), y1.cpu().numpy().view(np.uint32)), f"n={n}"
+        g1, g2 = y1.cpu().numpy(), y2.cpu().numpy()
+        assert_close(g2, ref, am, FMA_REL, what=f"v2 n={n}")
+        assert_close(g1, ref, am, FMA_REL, what=f"v1 n={n}")
+        assert_close(g2, g1.astype(np.float64), am, 2 * FMA_REL, what=f"v2 vs v1 n={n}")
 
 
 def test_moe_gate_up_v2_workload(h):

@@ -86,6 +86,12 @@ def _load():
     lib.oracle_moe_down_q8.restype = ctypes.c_int
     lib.oracle_moe_down_q8.argtypes = [ctypes.c_int, P, P, P, P, I64, I64, ctypes.c_int, ctypes.c_int,
                                        I64, I64, P, P, ctypes.c_int]
+    lib.oracle_e4m3_rn.restype = ctypes.c_uint8
+    lib.oracle_e4m3_rn.argtypes = [ctypes.c_float]
+    lib.oracle_e2m1_rn.restype = ctypes.c_uint8
+    lib.oracle_e2m1_rn.argtypes = [ctypes.c_float]
+    lib.oracle_quantize_nvfp4_v2.restype = ctypes.c_int
+    lib.oracle_quantize_nvfp4_v2.argtypes = [P, I64, I64, P]
     lib.oracle_max_threads.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     _lib = lib
@@ -245,6 +251,30 @@ def quantize_q8_1(x, rows: int, k: int):
     if rc:
         raise ValueError(f"oracle_quantize_q8_1 failed ({rc})")
     return q, d
+
+
+def e4m3_rn(v: float) -> int:
+    """E4M3FN code nearest to v >= 0 (ties to even, saturating at 448)."""
+    return int(_load().oracle_e4m3_rn(float(v)))
+
+
+def e2m1_rn(v: float) -> int:
+    """E2M1 code nearest to v (ties to even, saturating at +-6, sign kept)."""
+    return int(_load().oracle_e2m1_rn(float(v)))
+
+
+def quantize_nvfp4_v2(x, rows: int, k: int) -> np.ndarray:
+    """x [rows][k] f32 -> NVFP4 V2 rows (uint8 [rows * k/32*18]): per 16 values
+    scale = E4M3 nearest to amax/6, codes = E2M1 nearest to x/scale, decided
+    in float32."""
+    xa = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+    if xa.size != rows * k:
+        raise ValueError("x has the wrong size")
+    out = np.empty(rows * row_bytes("nvfp4_v2", k), np.uint8)
+    rc = _load().oracle_quantize_nvfp4_v2(_ptr(xa), rows, k, _ptr(out))
+    if rc:
+        raise ValueError(f"oracle_quantize_nvfp4_v2 failed ({rc})")
+    return out
 
 
 def moe_gate_up_q8(fmt: str, mats, scales, q, d, in_f: int, n_ff: int, n_used: int, t: int,

@@ -640,6 +640,85 @@ int oracle_moe_down_q8(int fmt, const uint8_t *const *mats, const float *scales,
     return bad ? -1 : 0;
 }
 
+/* ---------------------------------------------------------------------- */
+/* NVFP4 activations for the block-scaled tensor-core product              */
+/* ---------------------------------------------------------------------- */
+
+/* The tensor cores' NVFP4 product (tcgen05 kind::mxf4nvf4) takes both
+ * operands as E2M1 values with one E4M3 scale per 16; the pages fix no rule
+ * for turning an f32 activation into that form (memra quantizes its
+ * activations to Q8_1, aprender's prefill names an FP8 activation scratch).
+ * Reading, the plainest one that keeps the activation's own NVFP4 groups:
+ * per block of 16 consecutive values of a row, scale = the E4M3 value nearest
+ * to amax/6 (6 being the largest E2M1 magnitude), code = the E2M1 value
+ * nearest to x/scale, both rounding to nearest with ties to the even code and
+ * saturating at the format's largest finite value; every step is one float32
+ * operation, so the codes are decided in float32.  A block whose scale
+ * rounds to zero gets zero codes.  The rows are written as NVFP4 V2 rows. */
+
+/* E4M3FN code (0x00..0x7E) nearest to v >= 0, ties to the even code,
+ * saturating at 448 (0x7E). */
+uint8_t oracle_e4m3_rn(float v) {
+    if (!(v > 0.0f)) return 0;
+    uint32_t best = 0;
+    double bd = fabs((double)v);
+    for (uint32_t c = 1; c <= 0x7Eu; ++c) {
+        double d = fabs(oracle_e4m3(c) - (double)v);
+        if (d < bd || (d == bd && (c & 1u) == 0)) {
+            best = c;
+            bd = d;
+        }
+    }
+    return (uint8_t)best;
+}
+
+/* E2M1 code (4 bits) nearest to v, ties to the even code, saturating at
+ * +-6; the sign bit is v's (a negative value that rounds to zero gives
+ * code 8, -0). */
+uint8_t oracle_e2m1_rn(float v) {
+    uint32_t sign = signbit(v) ? 8u : 0u;
+    double a = fabs((double)v);
+    uint32_t best = 0;
+    double bd = a;
+    for (uint32_t c = 1; c <= 7u; ++c) {
+        double d = fabs(oracle_e2m1(c) - a);
+        if (d < bd || (d == bd && (c & 1u) == 0)) {
+            best = c;
+            bd = d;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+/* x [rows][k] f32 -> rows of NVFP4 V2 ([rows][k/32*18] bytes: k/2 code
+ * bytes, element 2j in the low nibble of byte j, then k/16 scale bytes). */
+int oracle_quantize_nvfp4_v2(const float *x, int64_t rows, int64_t k, uint8_t *out) {
+    if (rows < 0 || k <= 0 || k % 32 != 0) return -1;
+    int64_t rb = k / 32 * 18;
+    for (int64_t r = 0; r < rows; ++r) {
+        uint8_t *row = out + r * rb;
+        memset(row, 0, (size_t)rb);
+        for (int64_t b = 0; b < k / 16; ++b) {
+            const float *xb = x + r * k + 16 * b;
+            float amax = 0.0f;
+            for (int j = 0; j < 16; ++j) {
+                float a = fabsf(xb[j]);
+                if (a > amax) amax = a;
+            }
+            float t = amax / 6.0f;
+            uint8_t sc = oracle_e4m3_rn(t);
+            float s = (float)oracle_e4m3(sc);
+            row[k / 2 + b] = sc;
+            for (int j = 0; j < 16; ++j) {
+                uint8_t c = (s == 0.0f) ? 0u : oracle_e2m1_rn(xb[j] / s);
+                int64_t e = 16 * b + j;
+                row[e / 2] |= (uint8_t)((e % 2 == 0) ? c : (c << 4));
+            }
+        }
+    }
+    return 0;
+}
+
 /* Threads an OpenMP region would use (1 when built without OpenMP). */
 int oracle_max_threads(void) {
 #ifdef _OPENMP

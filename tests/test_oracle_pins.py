@@ -7,6 +7,7 @@ against numpy / torch), a dropped or extra term or a transposed operand in the
 product (one-hot permutation, exact integer matmul, library matmul).
 """
 import math
+import os
 
 import numpy as np
 import pytest
@@ -538,3 +539,118 @@ def test_moe_down_q8_equals_the_float_path_on_exact_activations():
     h2[1] *= 2
     yg, _ = oracle.moe_down("nvfp4", mats, scales, h2, n_ff, gin, n_used, t)
     assert np.array_equal(y9, yg)
+
+
+# ---- NVFP4 activations for the block-scaled tensor-core product -------------
+
+def _e2m1v(c):
+    return float(oracle.e2m1([c])[0])
+
+
+def _e4m3v(c):
+    return float(oracle.e4m3([c])[0])
+
+
+def _e2m1_rounding_cases():
+    cases = []
+    with open(os.path.join(os.path.dirname(__file__), "golden", "e2m1_rounding.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                v, c = line.split()
+                cases.append((float(v), int(c)))
+    return cases
+
+
+def test_e2m1_rn_hand_rounded_values():
+    cases = _e2m1_rounding_cases()
+    assert len(cases) >= 20
+    for v, code in cases:
+        assert oracle.e2m1_rn(v) == code, (v, code)
+
+
+def test_e2m1_rn_is_the_identity_on_the_grid():
+    for c in range(16):
+        v = _e2m1v(c)
+        got = oracle.e2m1_rn(v)
+        assert got == c or (c in (0, 8) and got in (0, 8) and math.copysign(1, v) == (-1 if got == 8 else 1)), c
+
+
+def test_e4m3_rn_identity_midpoints_and_saturation():
+    # every finite positive E4M3 value maps to its own code; the midpoint of
+    # two neighbours (exact in float32) maps to the code with mantissa bit 0,
+    # and a hair above or below it to the nearer one
+    vals = [_e4m3v(c) for c in range(0x7F)]
+    for c in range(0x7F):
+        assert oracle.e4m3_rn(vals[c]) == c, c
+    for c in range(0x7E):
+        mid = np.float32((vals[c] + vals[c + 1]) / 2)
+        assert float(mid) == (vals[c] + vals[c + 1]) / 2
+        even = c if c % 2 == 0 else c + 1
+        assert oracle.e4m3_rn(float(mid)) == even, hex(c)
+        up, down = np.nextafter(mid, np.float32(np.inf)), np.nextafter(mid, np.float32(0))
+        assert oracle.e4m3_rn(float(up)) == c + 1 and oracle.e4m3_rn(float(down)) == c, hex(c)
+    assert oracle.e4m3_rn(448.0) == 0x7E and oracle.e4m3_rn(1e30) == 0x7E and oracle.e4m3_rn(0.0) == 0
+
+
+def _v2_block(row, k, b):
+    """(scale code, 16 codes) of block b of one V2 row."""
+    codes = [(row[(16 * b + j) // 2] >> (4 * ((16 * b + j) % 2))) & 15 for j in range(16)]
+    return int(row[k // 2 + b]), codes
+
+
+def test_quantize_nvfp4_hand_blocks():
+    k = 64
+    x = np.zeros((1, k), np.float32)
+    # block 0: amax 6 -> amax/6 = 1.0 exactly, E4M3 0x38; the values are on the grid
+    x[0, :6] = [6.0, -3.0, 1.5, 0.5, 0.0, -0.25]
+    # block 1: the same values doubled -> scale 2.0 (0x40), the same codes
+    x[0, 16:22] = [12.0, -6.0, 3.0, 1.0, 0.0, -0.5]
+    # block 2: all zeros -> scale 0 and zero codes
+    # block 3: amax 1 -> 1/6 rounds to 1.375 * 2^-3 = 0.171875 (0x23); 1/0.171875
+    # = 5.818... rounds to 6 (code 7), 0.5/0.171875 = 2.909... to 3 (code 5)
+    x[0, 48:51] = [1.0, 0.5, -0.1]
+    row = oracle.quantize_nvfp4_v2(x, 1, k)
+    assert row.size == k // 32 * 18
+    assert _v2_block(row, k, 0) == (0x38, [7, 13, 3, 1, 0, 8] + [0] * 10)
+    assert _v2_block(row, k, 1) == (0x40, [7, 13, 3, 1, 0, 8] + [0] * 10)
+    assert _v2_block(row, k, 2) == (0x00, [0] * 16)
+    # -0.1 / 0.171875 = -0.58 -> -0.5 (code 9)
+    assert _v2_block(row, k, 3) == (0x23, [7, 5, 9] + [0] * 13)
+
+
+def test_quantize_nvfp4_round_trip_and_error_bound_on_random_rows():
+    rng = np.random.default_rng(11)
+    rows, k = 5, 256
+    x = rng.uniform(-1, 1, (rows, k)).astype(np.float32)
+    x[1] *= 40.0
+    x[2, :16] = 0.0
+    q = oracle.quantize_nvfp4_v2(x, rows, k)
+    xq = oracle.dequant("nvfp4_v2", q, rows, k)
+    rb = k // 32 * 18
+    for r in range(rows):
+        row = q[r * rb:(r + 1) * rb]
+        for b in range(k // 16):
+            sc, codes = _v2_block(row, k, b)
+            s = _e4m3v(sc)
+            blk = x[r, 16 * b:16 * b + 16].astype(np.float64)
+            amax = np.abs(blk).max()
+            # the scale is the E4M3 value nearest amax/6: no code is nearer
+            t = float(np.float32(amax) / np.float32(6))
+            assert all(abs(_e4m3v(c) - t) >= abs(s - t) for c in range(0x7F))
+            for j in range(16):
+                v = blk[j]
+                got = xq[r, 16 * b + j]
+                assert got == _e2m1v(codes[j]) * s
+                if s == 0:
+                    assert got == 0
+                    continue
+                a = abs(v) / s
+                # E2M1 gap at this magnitude (0.5 below 2, 1 below 4, 2 above);
+                # past 6 the value saturates
+                gap = 0.5 if a < 2 else (1.0 if a < 4 else 2.0)
+                assert abs(v - got) <= (gap / 2) * s * (1 + 1e-6) or (a > 6 and abs(got) == 6 * s)
+    # values already on the grid with scale 1 come back exactly
+    g = np.array([[6, -4, 3, -2, 1.5, -1, 0.5, 0, 6, 4, -3, 2, -1.5, 1, -0.5, 0]], np.float32)
+    assert np.array_equal(oracle.dequant("nvfp4_v2", oracle.quantize_nvfp4_v2(g.repeat(2, 1), 1, 32), 1, 32),
+                          g.repeat(2, 1))

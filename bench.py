@@ -620,7 +620,7 @@ def run_sub_benches(q, lib, h, torch, synth, stream, hbm_gbs):
     out = {"timing": f"median over {ROUNDS} rounds of back-to-back calls (weights rotated through more "
                      "than 2x the L2 size)",
            "gemv": [], "moe": None, "moe_q8": None, "moe_v2": None, "repack_v2": None, "moe_down": None,
-           "moe_down_q8": None, "dequant": []}
+           "moe_down_q8": None, "dequant": [], "fp4": None}
     # GEMV: rotate over enough weight copies to exceed L2 several times
     for fmt in ("q4_k", "q8_0"):
         for m, k in ((4608, 1024), (1024, 4608)):
@@ -755,10 +755,98 @@ def run_sub_benches(q, lib, h, torch, synth, stream, hbm_gbs):
                                        "frac_hbm": f})
             except Exception as exc:
                 out["dequant"].append({"dtype": "nvfp4_v2", "error": f"{type(exc).__name__}: {exc}"})
+    try:
+        out["fp4"] = _fp4_sub(q, lib, h, torch, synth, stream, hbm_gbs)
+    except Exception as exc:  # reported in the JSON line, never fatal to the headline measurement
+        out["fp4"] = {"error": f"{type(exc).__name__}: {exc}"}
     st = q.qmm_sync_status(h)
     if st != 0:
         raise RuntimeError(f"device status {st} in the sub-benchmarks")
     return out
+
+
+# nominal dense FP4 (NVFP4 block-scaled) over bf16 tensor rate: 13.5 / 2.25
+FP4_OVER_BF16 = 13.5 / 2.25
+
+
+def _fp4_sub(q, lib, h, torch, synth, stream, hbm_gbs):
+    """The block-scaled FP4 prefill on the four 512-token shapes: weights from
+    the NVFP4 stream repacked to V2 rows by the library, each call quantizing
+    its f32 activation (qmm_quantize_nvfp4) and running qmm_gemm_fp4."""
+    sptr = stream.cuda_stream
+    _, f16_tflops, _ = _peaks()
+    fp4_tflops = f16_tflops * FP4_OVER_BF16
+    copies = 4
+    items = []
+    for label, m, k in SHAPES:
+        rb = q.qmm_row_bytes("nvfp4_v2", k)
+        v1 = torch.from_numpy(synth.nvfp4_rows(0x4F00 + m, m, k)).cuda()
+        sets = []
+        for _ in range(copies):
+            w2 = torch.empty(m * rb, dtype=torch.uint8, device="cuda")
+            if lib.qmm_nvfp4_repack_v2(h, v1.data_ptr(), w2.data_ptr(), m, k, sptr) != 0:
+                raise RuntimeError("qmm_nvfp4_repack_v2 refused the call")
+            sets.append({"w": w2, "x": torch.from_numpy(synth.activations(N_TOKENS, k)).cuda(),
+                         "xq": torch.empty(N_TOKENS * rb, dtype=torch.uint8, device="cuda"),
+                         "d": torch.empty(N_TOKENS, m, dtype=torch.float32, device="cuda")})
+        flops = 2.0 * m * k * N_TOKENS
+        byts = m * rb + 4 * N_TOKENS * k + 2 * N_TOKENS * rb + 4 * N_TOKENS * m
+        items.append({"label": label, "m": m, "k": k, "sets": sets, "flops": flops, "bytes": byts})
+
+    def call(it, c):
+        s = it["sets"][c]
+        st = lib.qmm_quantize_nvfp4(h, s["x"].data_ptr(), s["xq"].data_ptr(), N_TOKENS, it["k"], sptr)
+        st = st or lib.qmm_gemm_fp4(h, s["w"].data_ptr(), s["xq"].data_ptr(), s["d"].data_ptr(), it["m"], it["k"],
+                                   N_TOKENS, sptr)
+        if st:
+            raise RuntimeError(f"fp4 call status {st}")
+
+    for c in range(copies):
+        for it in items:
+            call(it, c)
+    torch.cuda.synchronize()
+    # per call (quantize + GEMM) with an event pair around each; then the
+    # four calls back to back as a step
+    steps = 50
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in items]
+           for _ in range(steps)]
+    for s_ in range(steps):
+        torch.cuda._sleep(1_000_000)
+        for i, it in enumerate(items):
+            evs[s_][i][0].record(stream)
+            call(it, s_ % copies)
+            evs[s_][i][1].record(stream)
+    torch.cuda.synchronize()
+    per = []
+    tot_us, tot_ideal = 0.0, 0.0
+    for i, it in enumerate(items):
+        us = _med([evs[s_][i][0].elapsed_time(evs[s_][i][1]) for s_ in range(steps)]) * 1e3
+        t_t = it["flops"] / (fp4_tflops * 1e12)
+        t_h = it["bytes"] / (hbm_gbs * 1e9)
+        ideal = max(t_t, t_h) * 1e6
+        tot_us += us
+        tot_ideal += ideal
+        per.append({"shape": it["label"], "us": round(us, 3), "tflops": round(it["flops"] / (us * 1e-6) / 1e12, 1),
+                    "bound": "tensor" if t_t >= t_h else "hbm", "ideal_us": round(ideal, 3),
+                    "frac": round(ideal / us, 4)})
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    step_ms = []
+    for s_ in range(steps):
+        torch.cuda._sleep(1_000_000)
+        ev0.record(stream)
+        for it in items:
+            call(it, s_ % copies)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        step_ms.append(ev0.elapsed_time(ev1))
+    fl = sum(it["flops"] for it in items)
+    ms = _med(step_ms)
+    return {"workload": "the four 512-token shapes, W NVFP4 V2 rows, X quantized to NVFP4 per call",
+            "launches_per_call": 2, "per_gemm": per, "step_us": round(ms * 1e3, 3),
+            "step_tflops": round(fl / (ms * 1e-3) / 1e12, 1),
+            "frac": round(tot_ideal / tot_us, 4),
+            "peak": f"FP4 {fp4_tflops:.0f} TFLOP/s = measured bf16 x {FP4_OVER_BF16:.0f} (nominal ratio); "
+                    f"HBM {hbm_gbs} GB/s; per GEMM the slower of the two"}
 
 
 def run_profile_gemv(args):

@@ -7,7 +7,7 @@ loaded, importing the functions raises.
 
 Names follow the C ABI: ``qmm_create``, ``qmm_destroy``, ``qmm_gemm``,
 ``qmm_gemv``, ``qmm_moe_gemv``, ``qmm_moe_down``, ``qmm_quantize_q8_1``, ``qmm_moe_gemv_q8``,
-``qmm_moe_down_q8``, ``qmm_nvfp4_repack_v2``, ``qmm_dequant``, ``qmm_sync_status``,
+``qmm_moe_down_q8``, ``qmm_quantize_nvfp4``, ``qmm_gemm_fp4``, ``qmm_nvfp4_repack_v2``, ``qmm_dequant``, ``qmm_sync_status``,
 ``qmm_row_bytes``, ``qmm_gemm_workspace_bytes``, ``qmm_moe_down_workspace_bytes``,
 ``qmm_strerror``.
 """
@@ -32,7 +32,7 @@ STATUS = {0: "QMM_OK", 1: "QMM_ERR_INVALID_ARG", 2: "QMM_ERR_UNSUPPORTED", 3: "Q
 EXPORTS = ("qmm_create", "qmm_destroy", "qmm_strerror", "qmm_block_weights", "qmm_block_bytes",
            "qmm_row_bytes", "qmm_gemm_workspace_bytes", "qmm_gemm", "qmm_gemv", "qmm_moe_gemv",
            "qmm_moe_down_workspace_bytes", "qmm_moe_down", "qmm_nvfp4_repack_v2", "qmm_quantize_q8_1",
-           "qmm_moe_gemv_q8", "qmm_moe_down_q8",
+           "qmm_moe_gemv_q8", "qmm_moe_down_q8", "qmm_quantize_nvfp4", "qmm_gemm_fp4",
            "qmm_dequant", "qmm_sync_status", "qmm_gemm_noalloc", "qmm_gemm_noalloc_status",
            "qmm_testing_set_wait_limit_ns",
            "qmm_testing_skip_first_stage_load")
@@ -74,6 +74,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "qmm_moe_down": (I, [P, I, P, P, P, P, I64, I64, I, I, P, SZ, P]),
         "qmm_dequant": (I, [P, I, P, P, I64, I64, ctypes.c_float, P]),
         "qmm_quantize_q8_1": (I, [P, P, P, P, I64, I64, P]),
+        "qmm_quantize_nvfp4": (I, [P, P, P, I64, I64, P]),
+        "qmm_gemm_fp4": (I, [P, P, P, P, I64, I64, I64, P]),
         "qmm_moe_gemv_q8": (I, [P, I, P, P, P, P, P, I64, I64, I, I, P]),
         "qmm_moe_down_q8": (I, [P, I, P, P, P, P, P, I64, I64, I, I, P, SZ, P]),
         "qmm_nvfp4_repack_v2": (I, [P, P, P, I64, I64, P]),
@@ -204,6 +206,14 @@ def qmm_moe_down_q8(h, t, w_ptrs, scales, q, d, y, n_ff, gin, n_used, t_tokens, 
     _check(load().qmm_moe_down_q8(h, _dt(t), _ptr(w_ptrs), _ptr(scales), _ptr(q), _ptr(d), _ptr(y), n_ff, gin,
                                   n_used, t_tokens, _ptr(workspace), workspace_bytes, _stream(stream)),
            "qmm_moe_down_q8")
+
+
+def qmm_quantize_nvfp4(h, x, xq, rows, k, stream=None) -> None:
+    _check(load().qmm_quantize_nvfp4(h, _ptr(x), _ptr(xq), rows, k, _stream(stream)), "qmm_quantize_nvfp4")
+
+
+def qmm_gemm_fp4(h, w, xq, dst, m, k, n, stream=None) -> None:
+    _check(load().qmm_gemm_fp4(h, _ptr(w), _ptr(xq), _ptr(dst), m, k, n, _stream(stream)), "qmm_gemm_fp4")
 
 
 def qmm_nvfp4_repack_v2(h, v1, v2, m, k, stream=None) -> None:

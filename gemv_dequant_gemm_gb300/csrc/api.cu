@@ -140,6 +140,7 @@ int qmm_create(int device, qmm_handle *out) {
         cudaError_t e = cudaMalloc(&h->d_status, sizeof(uint32_t));
         if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, sizeof(uint32_t));
         if (e == cudaSuccess) e = qmm::gemm_tc_init();
+        if (e == cudaSuccess) e = qmm::gemm_fp4_init();
         return e;
     });
     if (st != QMM_OK) {
@@ -340,6 +341,33 @@ int qmm_moe_down_q8(qmm_handle h, qmm_dtype t, const void *const *w_ptrs, const 
                                            static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess || n_used == 1) return e;
         return qmm::launch_moe_combine(part, y, gin, n_used, t_tokens, h->num_sms, static_cast<cudaStream_t>(stream));
+    });
+}
+
+int qmm_quantize_nvfp4(qmm_handle h, const float *x, void *xq, int64_t rows, int64_t k, void *stream) {
+    if (!valid_handle(h) || !x || !xq) return QMM_ERR_INVALID_ARG;
+    if (rows < 1 || rows > kMaxMN || k < 256 || k > kMaxK || k % 256 != 0) return QMM_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(xq)) return QMM_ERR_ALIGN;
+    if (overlaps(xq, static_cast<size_t>(rows * qmm_row_bytes(QMM_NVFP4_V2, k)), x,
+                 static_cast<size_t>(rows * k) * sizeof(float)))
+        return QMM_ERR_OVERLAP;
+    return on_device(h, [&] {
+        return qmm::launch_quantize_nvfp4(x, xq, rows, k, h->num_sms, static_cast<cudaStream_t>(stream));
+    });
+}
+
+int qmm_gemm_fp4(qmm_handle h, const void *w, const void *xq, float *dst, int64_t m, int64_t k, int64_t n,
+                 void *stream) {
+    if (!valid_handle(h) || !w || !xq || !dst) return QMM_ERR_INVALID_ARG;
+    if (m < 1 || n < 1 || m > kMaxMN || n > kMaxMN || k < 256 || k > kMaxK || k % 256 != 0) return QMM_ERR_SHAPE;
+    if (!aligned16(w) || !aligned16(xq) || !aligned16(dst)) return QMM_ERR_ALIGN;
+    const int64_t rb = qmm_row_bytes(QMM_NVFP4_V2, k);
+    const size_t dbytes = static_cast<size_t>(n * m) * sizeof(float);
+    if (overlaps(dst, dbytes, w, static_cast<size_t>(rb * m)) || overlaps(dst, dbytes, xq, static_cast<size_t>(rb * n)))
+        return QMM_ERR_OVERLAP;
+    return on_device(h, [&] {
+        return qmm::launch_gemm_fp4(w, xq, dst, m, k, n, h->num_sms, h->d_status, h->wait_limit_ns,
+                                    static_cast<cudaStream_t>(stream));
     });
 }
 

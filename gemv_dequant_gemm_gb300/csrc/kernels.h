@@ -51,6 +51,16 @@ cudaError_t launch_moe_q8(int dtype, const void *const *w_ptrs, int64_t rb, cons
                           const float *d, float *dst, int64_t k, int64_t rows_per_mat, int mats, int n_pairs,
                           int n_used, int num_sms, uint32_t *status, uint64_t limit_ns, cudaStream_t st);
 
+// Activation rows [rows][k] f32 -> NVFP4 V2 rows (E2M1 codes, one E4M3 scale
+// per 16, nearest values, decided in float32); k % 256 == 0.
+cudaError_t launch_quantize_nvfp4(const float *x, void *out, int64_t rows, int64_t k, int num_sms, cudaStream_t st);
+
+// dst[n][m] = sum_k W[m][k] Xq[n][k], W and Xq NVFP4 V2 rows, on the
+// block-scaled FP4 tensor cores; k % 256 == 0.
+cudaError_t launch_gemm_fp4(const void *w, const void *xq, float *dst, int64_t m, int64_t k, int64_t n, int num_sms,
+                            uint32_t *status, uint64_t limit_ns, cudaStream_t st);
+cudaError_t gemm_fp4_init();
+
 // NVFP4 36-byte-group rows -> V2 rows (codes, then the scale stream); k % 64 == 0.
 cudaError_t launch_nvfp4_repack_v2(const uint8_t *v1, uint8_t *v2, int64_t m, int64_t k, int num_sms,
                                    cudaStream_t st);

@@ -257,6 +257,41 @@ int qmm_moe_down_q8(qmm_handle h, qmm_dtype t, const void *const *w_ptrs, const 
                     const int8_t *q, const float *d, float *y, int64_t n_ff, int64_t gin, int n_used,
                     int t_tokens, void *workspace, size_t workspace_bytes, void *stream);
 
+/* Activation rows for the block-scaled FP4 product (qmm_gemm_fp4): x
+ * [rows][k] float32 becomes NVFP4 V2 rows xq (rows * qmm_row_bytes(
+ * QMM_NVFP4_V2, k) bytes: k/2 code bytes, element 2j in the low nibble of
+ * byte j, then k/16 E4M3 scale bytes).  Per block of 16 consecutive values:
+ * scale = the E4M3 value nearest amax/6, code = the E2M1 value nearest
+ * x/scale, ties to the even code, both saturating at the format's largest
+ * finite value (448, 6); zero codes when the scale is zero.  Every step is a
+ * float32 operation, so the bytes match any IEEE implementation of the same
+ * steps.  The pages fix no activation rule for an FP4 tensor-core product
+ * (memra-engine 0.128.0 moe_rows_ceiling_bench.rs keeps its weights in NVFP4
+ * and quantizes its activation to Q8_1; aprender-serve 0.70.2
+ * cublas_prefill/mod.rs names an FP8 activation scratch for its low-precision
+ * GEMM): this is the plainest reading, the activation in the weights' own
+ * NVFP4 groups.  Useful range: |x| <= 2688 (6 * 448); blocks whose amax/6 is
+ * below 2^-10 quantize to zero.  1 <= rows <= 2^24, 256 <= k <= 2^20, k % 256
+ * == 0; device pointers, 16-byte aligned, not overlapping.  Errors:
+ * QMM_ERR_INVALID_ARG, QMM_ERR_SHAPE, QMM_ERR_ALIGN, QMM_ERR_OVERLAP,
+ * QMM_ERR_CUDA. */
+int qmm_quantize_nvfp4(qmm_handle h, const float *x, void *xq, int64_t rows, int64_t k, void *stream);
+
+/* The prefill product on the block-scaled FP4 tensor cores (tcgen05
+ * kind::mxf4nvf4): dst[n][m] = sum_k W[m][k] * Xq[n][k] with W [m][k] and Xq
+ * [n][k] both NVFP4 V2 rows (weights repacked from 36-byte groups by
+ * qmm_nvfp4_repack_v2, activations written by qmm_quantize_nvfp4).  Each
+ * product of two E2M1 values and each 16-term block sum is exact; the block
+ * sums are scaled by the two E4M3 scales and accumulated in fp32.  Accuracy
+ * |dst - exact| <= 2e-3 * sum_k |W * Xq| + 1e-6 against the exact product on
+ * the quantized activation (the tensor-core tolerance).  1 <= m, n <= 2^24,
+ * 256 <= k <= 2^20, k % 256 == 0; device pointers, 16-byte aligned, dst
+ * overlapping neither input.  Errors: QMM_ERR_INVALID_ARG, QMM_ERR_SHAPE,
+ * QMM_ERR_ALIGN, QMM_ERR_OVERLAP, QMM_ERR_CUDA; device-side timeouts through
+ * qmm_sync_status. */
+int qmm_gemm_fp4(qmm_handle h, const void *w, const void *xq, float *dst, int64_t m, int64_t k, int64_t n,
+                 void *stream);
+
 /* Repack NVFP4 rows into the V2 layout (memra-engine 0.128.0
  * src/bin/moe_rows_ceiling_bench.rs, main: the V2 arms read the same values
  * through rows repacked with the scales split out).  v1 is [m] rows of

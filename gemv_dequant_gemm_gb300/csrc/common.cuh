@@ -338,6 +338,70 @@ template <int V> __device__ __forceinline__ float warp_transpose_sum(float (&a)[
     return a[0];
 }
 
+// Split-K epilogue of the tensor-core GEMMs: CTA z of a cluster of S sums
+// column slice z (BN/S columns) of the S partial tiles, each [BN][ROWS] fp32
+// at shared address red0 in every CTA of the cluster, in rank order 0..S-1,
+// and stores it to dst[n][m] (row stride M).  Work items are 4 consecutive
+// rows of one column, spread over nthreads threads; each thread keeps 16/S
+// items' remote loads in flight before it sums any (a remote load costs
+// hundreds of cycles).  skip: store nothing (a CTA of the cluster gave up).
+template <int S, int ROWS>
+__device__ __forceinline__ void splitk_reduce_store_s(uint32_t red0, int z, int BN, int m0, int n0, int M, int N,
+                                                      float *dst, int tid, int nthreads, bool skip) {
+    constexpr int B = 16 / S;  // items in flight per thread
+    const int cols = BN / S, c0 = z * cols;
+    const int total = skip ? 0 : cols * (ROWS / 4);
+    const bool vec = (M % 4) == 0;
+    for (int it0 = tid; it0 < total; it0 += B * nthreads) {
+        float4 v[B][S];
+#pragma unroll
+        for (int u = 0; u < B; ++u) {
+            const int it = it0 + u * nthreads;
+            if (it < total) {
+                const int cl = c0 + it / (ROWS / 4), r4 = (it % (ROWS / 4)) * 4;
+                const uint32_t off = static_cast<uint32_t>((cl * ROWS + r4) * 4);
+#pragma unroll
+                for (int pr = 0; pr < S; ++pr) v[u][pr] = ld_dsmem_v4(mapa_shared(red0 + off, static_cast<uint32_t>(pr)));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < B; ++u) {
+            const int it = it0 + u * nthreads;
+            if (it >= total) continue;
+            const int cl = c0 + it / (ROWS / 4), r4 = (it % (ROWS / 4)) * 4;
+            float4 acc = v[u][0];
+#pragma unroll
+            for (int pr = 1; pr < S; ++pr) {
+                acc.x += v[u][pr].x;
+                acc.y += v[u][pr].y;
+                acc.z += v[u][pr].z;
+                acc.w += v[u][pr].w;
+            }
+            const int gn = n0 + cl, gm = m0 + r4;
+            if (gn < N && gm < M) {
+                float *d = dst + static_cast<int64_t>(gn) * M + gm;
+                if (vec && gm + 4 <= M) {
+                    *reinterpret_cast<float4 *>(d) = acc;
+                } else {
+                    const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+                    for (int t = 0; t < 4 && gm + t < M; ++t) d[t] = a4[t];
+                }
+            }
+        }
+    }
+}
+
+// The same for a runtime S in {2, 4, 8}.
+template <int ROWS>
+__device__ __forceinline__ void splitk_reduce_store(uint32_t red0, int S, int z, int BN, int m0, int n0, int M, int N,
+                                                    float *dst, int tid, int nthreads, bool skip) {
+    switch (S) {
+    case 2: splitk_reduce_store_s<2, ROWS>(red0, z, BN, m0, n0, M, N, dst, tid, nthreads, skip); break;
+    case 4: splitk_reduce_store_s<4, ROWS>(red0, z, BN, m0, n0, M, N, dst, tid, nthreads, skip); break;
+    default: splitk_reduce_store_s<8, ROWS>(red0, z, BN, m0, n0, M, N, dst, tid, nthreads, skip); break;
+    }
+}
+
 // Launch `kernel` on `st` with programmatic dependent launch allowed (and an
 // optional cluster shape; 1 x 1 x 1 launches without clusters).
 template <typename... KArgs, typename... Args>

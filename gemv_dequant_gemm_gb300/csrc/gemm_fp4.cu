@@ -13,7 +13,8 @@
 // a 16-term block sum is exact, it is scaled by the two E4M3 scales and
 // accumulated in fp32 in tensor memory.
 //
-// CTA = one 128 (m) x 128 (n) output tile, k in 256-wide stages:
+// CTA = one 128 (m) x 128 (n) output tile, k in 256-wide stages (split
+// over a cluster of up to 8 CTAs when the tiles alone do not cover the SMs):
 //   warp 0      TMA producer: per stage the W and X code tiles (128 rows x
 //               128 bytes each, 128-byte swizzle: the K-major operand layout)
 //               and the W and X scale tiles (128 rows x 16 bytes);
@@ -23,8 +24,10 @@
 //               the MMA's scale layout (rows 32i + j in column i of lane j,
 //               the same in every lane quarter, four columns per MMA), one
 //               tcgen05.st of 16 columns per operand and warp; then the
-//               epilogue: tcgen05.ld of the fp32 accumulator, stores of
-//               dst[n][m] (m contiguous).
+//               epilogue: tcgen05.ld of the fp32 accumulator into shared
+//               memory as [n][m], one TMA store of the tile (split-K: a
+//               fixed-order sum of the cluster's partial tiles through
+//               distributed shared memory, no atomics).
 // Every wait is bounded; a wait that runs out latches the timeout bit and
 // the CTA stops issuing work, waits for its copies and MMAs in flight, frees
 // its tensor memory and returns without storing.
@@ -73,6 +76,8 @@ constexpr uint32_t IDESC = (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >>
 struct Params {
     float *dst;
     int M, N, K;
+    int splits;  // CTAs per output tile (a cluster along z), each a contiguous share of the k stages
+    int dtma;    // 1: the tile is stored with one TMA store through map_d (M % 4 == 0)
     uint32_t *status;
     uint64_t limit_ns;
 };
@@ -105,14 +110,18 @@ __device__ __forceinline__ bool f4_wait_drain(uint64_t *bar, uint32_t parity, ui
 __global__ void __launch_bounds__(f4::THREADS, 1)
     gemm_fp4_kernel(const __grid_constant__ CUtensorMap map_wc, const __grid_constant__ CUtensorMap map_ws,
                     const __grid_constant__ CUtensorMap map_xc, const __grid_constant__ CUtensorMap map_xs,
-                    const f4::Params p) {
+                    const __grid_constant__ CUtensorMap map_d, const f4::Params p) {
     using namespace f4;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Ctl *ctl = reinterpret_cast<Ctl *>(base + STAGES * STAGE);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
-    const int NK = p.K / KS;
+    const int S = p.splits;
+    const int z = (S > 1) ? static_cast<int>(cluster_rank()) : 0;
+    const int kt0 = z * (p.K / KS) / S, kt1 = (z + 1) * (p.K / KS) / S;
+    const int NK = kt1 - kt0;  // this CTA's stages (>= 1)
+    float *sRed = reinterpret_cast<float *>(base);  // the fp32 tile [BN][BM], after the main loop
     // stage s: [W codes][X codes][W scales][X scales]
     auto wc = [&](int s) { return base + s * STAGE; };
     auto xc = [&](int s) { return base + s * STAGE + CODE_TILE; };
@@ -154,7 +163,7 @@ __global__ void __launch_bounds__(f4::THREADS, 1)
                 const uint32_t ph = (i / STAGES) & 1;
                 if (!mbar_wait_bounded(&ctl->empty[s], ph ^ 1, abort, p.status, p.limit_ns)) break;
                 mbar_arrive_expect_tx(&ctl->full[s], STAGE);
-                const int kx = i * (KS / 2), ksx = i * (KS / 16);  // byte coordinates of the stage
+                const int kx = (kt0 + i) * (KS / 2), ksx = (kt0 + i) * (KS / 16);  // byte coordinates of the stage
                 tma_load_2d(wc(s), &map_wc, kx, m0, &ctl->full[s]);
                 tma_load_2d(xc(s), &map_xc, kx, n0, &ctl->full[s]);
                 tma_load_2d(wsc(s), &map_ws, ksx, m0, &ctl->full[s]);
@@ -221,30 +230,61 @@ __global__ void __launch_bounds__(f4::THREADS, 1)
     }
 
     // ---------------- epilogue (warps 2-5) ----------------
-    if (warp >= 2) {
+    // The fp32 tile goes through shared memory as [BN][BM] (m contiguous; the
+    // stage ring is free once every MMA has completed), then one TMA store;
+    // with split-K the CTAs of a cluster each sum a column slice of all the
+    // partial tiles in rank order through distributed shared memory.
+    const bool is_epi = warp >= 2;
+    bool have = false;
+    if (is_epi) {
         const bool drained = f4_wait_drain(&ctl->accum, 0, p.status, p.limit_ns);
         if (warp == 2 && lane == 0) griddep_launch();
         if (!drained) *abort = 1;
-        const bool have = __all_sync(0xFFFFFFFFu, drained && !*abort);
+        have = __all_sync(0xFFFFFFFFu, drained && !*abort);
         if (have) {
             tc_fence_after();
             const int q = warp & 3;
-            const int gm = m0 + 32 * q + lane;
+            const int r = 32 * q + lane;  // tile row (m)
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + 32 * c, v);
                 tmem_ld_wait();
-                const int gn0 = n0 + 32 * c;
-                if (gm < p.M) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (gn0 + j < p.N) p.dst[static_cast<int64_t>(gn0 + j) * p.M + gm] = __uint_as_float(v[j]);
-                }
+                for (int j2 = 0; j2 < 32; ++j2) sRed[(32 * c + j2) * BM + r] = __uint_as_float(v[j2]);
             }
         }
     } else if (threadIdx.x == 0) {
         griddep_launch();
+    }
+    if (S == 1) {
+        if (is_epi) {
+            fence_proxy_async_smem();  // the generic-proxy writes above, before the TMA store reads them
+            asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
+            if (p.dtma) {
+                if (warp == 2 && lane == 0 && !*abort) {
+                    tma_store_2d(&map_d, m0, n0, sRed);
+                    bulk_commit_group();
+                    bulk_wait_group_read0();  // the source stays valid until the engine has read it
+                }
+            } else if (!*abort) {
+                const int et = threadIdx.x - 64;  // 0..127
+                for (int it = et; it < BN * BM; it += 128) {
+                    const int cl = it / BM, rr = it % BM;
+                    const int gn = n0 + cl, gm = m0 + rr;
+                    if (gn < p.N && gm < p.M) p.dst[static_cast<int64_t>(gn) * p.M + gm] = sRed[cl * BM + rr];
+                }
+            }
+        }
+    } else {
+        __syncwarp();
+        cluster_sync_all();
+        int any_abort = 0;
+        for (int pr = 0; pr < S; ++pr) any_abort |= ld_dsmem_u32(mapa_shared(smem_u32(&ctl->abort), pr));
+        splitk_reduce_store<BM>(smem_u32(sRed), S, z, BN, m0, n0, p.M, p.N, p.dst, static_cast<int>(threadIdx.x),
+                                   THREADS, any_abort != 0);
+        __syncwarp();
+        cluster_sync_all();  // peers keep their partials until every slice is read
     }
     tc_fence_before();
     __syncthreads();
@@ -350,7 +390,6 @@ cudaError_t launch_quantize_nvfp4(const float *x, void *out, int64_t rows, int64
 cudaError_t launch_gemm_fp4(const void *w, const void *xq, float *dst, int64_t m, int64_t k, int64_t n, int num_sms,
                             uint32_t *status, uint64_t limit_ns, cudaStream_t st) {
     using namespace f4;
-    (void)num_sms;
     const int64_t rb = k / 32 * 18;  // V2 row bytes of W and of Xq
     CUtensorMap mwc, mws, mxc, mxs;
     const uint8_t *wb = static_cast<const uint8_t *>(w), *xb = static_cast<const uint8_t *>(xq);
@@ -364,8 +403,30 @@ cudaError_t launch_gemm_fp4(const void *w, const void *xq, float *dst, int64_t m
     p.K = static_cast<int>(k);
     p.status = status;
     p.limit_ns = limit_ns;
-    const dim3 grid(static_cast<unsigned>((m + BM - 1) / BM), static_cast<unsigned>((n + BN - 1) / BN), 1);
-    return launch_pdl(gemm_fp4_kernel, grid, dim3(THREADS), SMEM, st, dim3(1, 1, 1), mwc, mws, mxc, mxs, p);
+    // split-K: enough CTAs per tile to cover the SMs, at most one per stage,
+    // a power of two up to 8 (it divides the tile width)
+    const int64_t tiles = ((m + BM - 1) / BM) * ((n + BN - 1) / BN);
+    int sp = 1;
+    while (sp < 8 && tiles * (sp * 2) <= num_sms && sp * 2 <= k / KS) sp *= 2;
+    p.splits = sp;
+    // dst [n][m] f32 as a TMA store target: boxes of [BN n][BM m]
+    CUtensorMap mdst;
+    memset(&mdst, 0, sizeof(mdst));
+    p.dtma = 0;
+    if (m % 4 == 0) {
+        auto fn = f4_encode_fn();
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(m), static_cast<cuuint64_t>(n)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(m) * 4};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(BM), static_cast<cuuint32_t>(BN)};
+        const cuuint32_t estr[2] = {1, 1};
+        p.dtma = fn && fn(&mdst, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, dst, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
+    const dim3 grid(static_cast<unsigned>((m + BM - 1) / BM), static_cast<unsigned>((n + BN - 1) / BN),
+                    static_cast<unsigned>(sp));
+    return launch_pdl(gemm_fp4_kernel, grid, dim3(THREADS), SMEM, st, dim3(1, 1, static_cast<unsigned>(sp)), mwc,
+                      mws, mxc, mxs, mdst, p);
 }
 
 }  // namespace qmm

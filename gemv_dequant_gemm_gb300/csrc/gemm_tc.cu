@@ -522,39 +522,8 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
         int any_abort = 0;
         for (int pr = 0; pr < S; ++pr) any_abort |= ld_dsmem_u32(mapa_shared(smem_u32(&ctl->abort), pr));
         // CTA z sums column slice z of the S partials in rank order and stores it
-        const int cols = BN / S;  // S divides BN (S is a power of two <= 8)
-        const int c0 = z * cols;
-        const uint32_t red0 = smem_u32(sRed);
-        const bool vec = (p.M % 4) == 0;
-        for (int it = any_abort ? cols * (ROWS / 4) : threadIdx.x; it < cols * (ROWS / 4); it += THREADS) {
-            const int cl = c0 + it / (ROWS / 4), r4 = (it % (ROWS / 4)) * 4;
-            const uint32_t off = static_cast<uint32_t>((cl * ROWS + r4) * 4);
-            // all peers' loads in flight first, then the sum in rank order
-            float4 v[MAX_SPLIT];
-#pragma unroll
-            for (int pr = 0; pr < MAX_SPLIT; ++pr)
-                if (pr < S) v[pr] = ld_dsmem_v4(mapa_shared(red0 + off, static_cast<uint32_t>(pr)));
-            float4 acc = v[0];
-#pragma unroll
-            for (int pr = 1; pr < MAX_SPLIT; ++pr) {
-                if (pr < S) {
-                    acc.x += v[pr].x;
-                    acc.y += v[pr].y;
-                    acc.z += v[pr].z;
-                    acc.w += v[pr].w;
-                }
-            }
-            const int gn = n0 + cl, gm = m0 + r4;
-            if (gn < p.N && gm < p.M) {
-                float *d = p.dst + static_cast<int64_t>(gn) * p.M + gm;
-                if (vec && gm + 4 <= p.M) {
-                    *reinterpret_cast<float4 *>(d) = acc;
-                } else {
-                    const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
-                    for (int t = 0; t < 4 && gm + t < p.M; ++t) d[t] = a4[t];
-                }
-            }
-        }
+        splitk_reduce_store<ROWS>(smem_u32(sRed), S, z, BN, m0, n0, p.M, p.N, p.dst,
+                                             static_cast<int>(threadIdx.x), THREADS, any_abort != 0);
         __syncwarp();
         cluster_sync_all();  // peers keep their partials until every slice is read
     }

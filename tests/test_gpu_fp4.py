@@ -88,7 +88,10 @@ def _exact_v2(rows, k, rng):
     return out.reshape(-1)
 
 
-@pytest.mark.parametrize("m,k,n", [(128, 256, 128), (256, 1024, 384), (300, 512, 200), (129, 768, 257)])
+# one tile; split-K over clusters of 2 and 4 with ragged tiles; 144 tiles with
+# m % 4 != 0 (no split, stores without the TMA store map); ffn_down's k
+@pytest.mark.parametrize("m,k,n", [(128, 256, 128), (256, 1024, 384), (300, 512, 200), (129, 768, 257),
+                                   (1027, 256, 2048), (256, 4608, 256)])
 def test_fp4_exact_arithmetic_is_bit_identical(h, m, k, n):
     rng = np.random.default_rng(m + k + n)
     w = _exact_v2(m, k, rng)

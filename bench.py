@@ -55,8 +55,8 @@ TF32_OVER_F16 = 1.1 / 2.25
 # bench reports null.
 GEMM_TRAFFIC_SOURCES = ("gemv_dequant_gemm_gb300/csrc/gemm_tc.cu", "gemv_dequant_gemm_gb300/csrc/decode.cuh",
                         "gemv_dequant_gemm_gb300/csrc/common.cuh")
-GEMM_TRAFFIC_SHA16 = "36d66afbb1831adc"
-GEMM_TRAFFIC_BYTES = 9.068e6
+GEMM_TRAFFIC_SHA16 = "dbc18318a2609380"
+GEMM_TRAFFIC_BYTES = 9.074e6
 
 
 def _gemm_traffic():
@@ -903,6 +903,55 @@ def run_profile_moe(args):
     return 0 if st == 0 else 1
 
 
+def run_profile_dequant(args):
+    """One dequant call repeated (a profiling run: not a bench line)."""
+    import torch
+
+    import gemv_dequant_gemm_gb300 as q
+    import synth
+    fmt, m, k = args.profile_dequant.split(",")
+    m, k = int(m), int(k)
+    torch.cuda.set_device(0)
+    h = q.qmm_create(0)
+    w = torch.from_numpy(synth.weights(fmt, m, k, m * q.qmm_row_bytes(fmt, k))).cuda()
+    out = torch.empty(m, k, dtype=torch.float32, device="cuda")
+    for _ in range(args.steps + args.warmup):
+        q.qmm_dequant(h, fmt, w, out, m, k)
+    torch.cuda.synchronize()
+    st = q.qmm_sync_status(h)
+    q.qmm_destroy(h)
+    print(json.dumps({"profile_dequant": args.profile_dequant, "status": st}))
+    return 0 if st == 0 else 1
+
+
+def run_profile_fp4(args):
+    """The FP4 prefill (quantize + GEMM) of one 512-token shape repeated (a
+    profiling run: not a bench line)."""
+    import torch
+
+    import gemv_dequant_gemm_gb300 as q
+    import synth
+    label = args.profile_fp4
+    _, m, k = [s for s in SHAPES if s[0] == label][0]
+    torch.cuda.set_device(0)
+    h = q.qmm_create(0)
+    rb = q.qmm_row_bytes("nvfp4_v2", k)
+    v1 = torch.from_numpy(synth.nvfp4_rows(0x4F00 + m, m, k)).cuda()
+    w2 = torch.empty(m * rb, dtype=torch.uint8, device="cuda")
+    q.qmm_nvfp4_repack_v2(h, v1, w2, m, k)
+    x = torch.from_numpy(synth.activations(N_TOKENS, k)).cuda()
+    xq = torch.empty(N_TOKENS * rb, dtype=torch.uint8, device="cuda")
+    d = torch.empty(N_TOKENS, m, dtype=torch.float32, device="cuda")
+    for _ in range(args.steps + args.warmup):
+        q.qmm_quantize_nvfp4(h, x, xq, N_TOKENS, k)
+        q.qmm_gemm_fp4(h, w2, xq, d, m, k, N_TOKENS)
+    torch.cuda.synchronize()
+    st = q.qmm_sync_status(h)
+    q.qmm_destroy(h)
+    print(json.dumps({"profile_fp4": label, "status": st}))
+    return 0 if st == 0 else 1
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -921,6 +970,10 @@ def main(argv=None):
                     help="call one GEMV shape warmup+steps times and exit (profiling runs)")
     ap.add_argument("--profile-moe", default=None, choices=["f32", "q8"],
                     help="call the NVFP4 MoE gate/up (f32 or Q8_1 activations) warmup+steps times and exit")
+    ap.add_argument("--profile-dequant", default=None, metavar="FMT,M,K",
+                    help="call one dequant shape warmup+steps times and exit (profiling runs)")
+    ap.add_argument("--profile-fp4", default=None, choices=[s[0] for s in SHAPES],
+                    help="call the FP4 prefill of one 512-token shape warmup+steps times and exit")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -928,6 +981,10 @@ def main(argv=None):
         return run_profile_gemv(args)
     if args.profile_moe:
         return run_profile_moe(args)
+    if args.profile_dequant:
+        return run_profile_dequant(args)
+    if args.profile_fp4:
+        return run_profile_fp4(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -314,10 +314,20 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
     return v;
 }
+// (no memory clobber either: the flags it reads are written before the first
+// cluster barrier; the loads may overlap the partial-tile loads that follow)
 __device__ __forceinline__ int ld_dsmem_u32(uint32_t addr) {
     int v;
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr));
     return v;
+}
+// The end of a split-K epilogue: this CTA's reads of its peers' shared memory
+// have returned (their values are in registers), so it arrives without
+// release semantics -- the arrival does not wait for its own global stores to
+// drain -- and then waits until every peer has done the same, so that no CTA
+// leaves while another still reads its partial tile.
+__device__ __forceinline__ void cluster_arrive_relaxed_wait() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
 }
 
 // Butterfly reduction of V values (a power of two <= 32) over the warp:
@@ -344,13 +354,14 @@ template <int V> __device__ __forceinline__ float warp_transpose_sum(float (&a)[
 // and stores it to dst[n][m] (row stride M).  Work items are 4 consecutive
 // rows of one column, spread over nthreads threads; each thread keeps 16/S
 // items' remote loads in flight before it sums any (a remote load costs
-// hundreds of cycles).  skip: store nothing (a CTA of the cluster gave up).
+// hundreds of cycles).  skip: store nothing (a CTA of the cluster gave up);
+// the loads still run, so they need not wait for the abort flags.
 template <int S, int ROWS>
 __device__ __forceinline__ void splitk_reduce_store_s(uint32_t red0, int z, int BN, int m0, int n0, int M, int N,
                                                       float *dst, int tid, int nthreads, bool skip) {
     constexpr int B = 16 / S;  // items in flight per thread
     const int cols = BN / S, c0 = z * cols;
-    const int total = skip ? 0 : cols * (ROWS / 4);
+    const int total = cols * (ROWS / 4);
     const bool vec = (M % 4) == 0;
     for (int it0 = tid; it0 < total; it0 += B * nthreads) {
         float4 v[B][S];
@@ -378,7 +389,7 @@ __device__ __forceinline__ void splitk_reduce_store_s(uint32_t red0, int z, int 
                 acc.w += v[u][pr].w;
             }
             const int gn = n0 + cl, gm = m0 + r4;
-            if (gn < N && gm < M) {
+            if (!skip && gn < N && gm < M) {
                 float *d = dst + static_cast<int64_t>(gn) * M + gm;
                 if (vec && gm + 4 <= M) {
                     *reinterpret_cast<float4 *>(d) = acc;

@@ -525,7 +525,7 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
         splitk_reduce_store<ROWS>(smem_u32(sRed), S, z, BN, m0, n0, p.M, p.N, p.dst,
                                              static_cast<int>(threadIdx.x), THREADS, any_abort != 0);
         __syncwarp();
-        cluster_sync_all();  // peers keep their partials until every slice is read
+        cluster_arrive_relaxed_wait();  // peers keep their partials until every slice is read
     }
     tc_fence_before();
     __syncthreads();

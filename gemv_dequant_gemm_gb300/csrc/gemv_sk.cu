@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(gs::MAX_THREADS) gemv_sk_kernel(const gs::Para
                 }
             }
         }
-        cluster_sync_all();  // peers keep their partials until every share is read
+        cluster_arrive_relaxed_wait();  // peers keep their partials until every share is read
     }
     if (!ok && tid == 0) {  // copies still in flight land before the CTA exits
         const uint64_t t0 = global_timer_ns();

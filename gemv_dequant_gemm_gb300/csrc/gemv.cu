@@ -465,6 +465,26 @@ template <int UW> __device__ __forceinline__ void load_xu(const float *xr, int64
     }
 }
 
+// Position of a CTA's current stage in its contiguous run of stages: matrix,
+// stage within the matrix, ring slot and ring phase, advanced stage by stage
+// without divisions.
+struct StageWalk {
+    int mat, sp, slot;
+    uint32_t ph;
+    __device__ __forceinline__ StageWalk(int s, int stages_per_mat)
+        : mat(s / stages_per_mat), sp(s - (s / stages_per_mat) * stages_per_mat), slot(0), ph(0) {}
+    __device__ __forceinline__ void next(int stages_per_mat, int ring) {
+        if (++sp == stages_per_mat) {
+            sp = 0;
+            ++mat;
+        }
+        if (++slot == ring) {
+            slot = 0;
+            ph ^= 1u;
+        }
+    }
+};
+
 template <int F, int NV, int JM>
 __global__ void __launch_bounds__(gr::THREADS, 1) gemv_rx_kernel(const gr::Params p) {
     using namespace gr;
@@ -513,17 +533,16 @@ __global__ void __launch_bounds__(gr::THREADS, 1) gemv_rx_kernel(const gr::Param
         // ---------------- producer: stage loads and the cross-warp sums ----------------
         const int wpt = p.tk / 32;  // warps per team
         int issued = 0;
+        StageWalk ld(s_begin, p.stages_per_mat), sw(s_begin, p.stages_per_mat);  // loads; sums (ring behind)
         for (int j = 0; j < nst + p.ring; ++j) {
-            const int slot = j % p.ring;
-            if (j >= p.ring || j >= nst) {
-                // the stage that used this slot, jr, has been consumed by every compute warp
-                const int jr = j - p.ring;
-                if (jr >= 0) {
-                    const bool ok = mbar_wait_bounded(&ctl->empty[slot], (jr / p.ring) & 1, abort, p.status, p.limit_ns);
+            const int slot = ld.slot;  // = j % ring, for the stage loaded and the one summed
+            if (j >= p.ring) {
+                // the stage that used this slot, jr = j - ring, has been consumed by every compute warp
+                {
+                    const bool ok = mbar_wait_bounded(&ctl->empty[slot], sw.ph, abort, p.status, p.limit_ns);
                     if (!__all_sync(0xFFFFFFFFu, ok)) break;
-                    const int s = s_begin + jr;
-                    const int mat = s / p.stages_per_mat;
-                    const int r0 = (s % p.stages_per_mat) * p.stage_rows;
+                    const int mat = sw.mat;
+                    const int r0 = sw.sp * p.stage_rows;
                     const int rows = min(p.stage_rows, p.rows_per_mat - r0);
                     const bool bad = ctl->bad[slot] != 0;
                     const float scale = !moe ? 1.0f : (table ? ctl->mscale[mat] : __ldg(p.scales + mat));
@@ -541,11 +560,11 @@ __global__ void __launch_bounds__(gr::THREADS, 1) gemv_rx_kernel(const gr::Param
                     }
                     if (bad && lane == 0) atomicOr(p.status, kDevBadPtr);
                 }
+                sw.next(p.stages_per_mat, p.ring);
             }
             if (j < nst && lane == 0) {
-                const int s = s_begin + j;
-                const int mat = s / p.stages_per_mat;
-                const int r0 = (s % p.stages_per_mat) * p.stage_rows;
+                const int mat = ld.mat;
+                const int r0 = ld.sp * p.stage_rows;
                 const int rows = min(p.stage_rows, p.rows_per_mat - r0);
                 const uint8_t *mp = !moe ? p.w : (table ? ctl->mptr[mat] : static_cast<const uint8_t *>(p.w_ptrs[mat]));
                 if (mp == nullptr || (reinterpret_cast<uintptr_t>(mp) & 15u) != 0) {
@@ -562,6 +581,7 @@ __global__ void __launch_bounds__(gr::THREADS, 1) gemv_rx_kernel(const gr::Param
                 }
             }
             if (j < nst) ++issued;
+            ld.next(p.stages_per_mat, p.ring);
             __syncwarp();
         }
         // on abort: copies still in flight land before the CTA exits
@@ -594,14 +614,17 @@ __global__ void __launch_bounds__(gr::THREADS, 1) gemv_rx_kernel(const gr::Param
                 cdoff[jj] = e0 >> 1;
             }
         }
-        int cur_tok = -1;
+        int cur_tok = -1, cur_mat = -1, tok = 0;
         bool dead = false;
-        for (int j = 0; j < nst; ++j) {
-            const int s = s_begin + j;
-            const int slot = j % p.ring;
-            const int mat = s / p.stages_per_mat;
-            const int tok = moe ? (mat % p.n_pairs) / p.n_used : 0;
-            if (tok != cur_tok) {  // uniform over the CTA: the stage decides it
+        StageWalk wk(s_begin, p.stages_per_mat);
+        for (int j = 0; j < nst; ++j, wk.next(p.stages_per_mat, p.ring)) {
+            const int slot = wk.slot;
+            const int mat = wk.mat;
+            if (mat != cur_mat) {  // uniform over the CTA: the stage decides it
+                cur_mat = mat;
+                tok = moe ? (mat % p.n_pairs) / p.n_used : 0;
+            }
+            if (tok != cur_tok) {
                 cur_tok = tok;
 #pragma unroll
                 for (int jj = 0; jj < JM; ++jj) {
@@ -622,9 +645,9 @@ __global__ void __launch_bounds__(gr::THREADS, 1) gemv_rx_kernel(const gr::Param
                     }
                 }
             }
-            const bool got = dead ? false : mbar_wait_bounded(&ctl->full[slot], (j / p.ring) & 1, abort, p.status, p.limit_ns);
+            const bool got = dead ? false : mbar_wait_bounded(&ctl->full[slot], wk.ph, abort, p.status, p.limit_ns);
             if (!__all_sync(0xFFFFFFFFu, got)) dead = true;
-            const int r0 = (s % p.stages_per_mat) * p.stage_rows;
+            const int r0 = wk.sp * p.stage_rows;
             const int rows = min(p.stage_rows, p.rows_per_mat - r0);
             const bool bad = !dead && ctl->bad[slot] != 0;
             const uint8_t *mp = !moe ? p.w : (table ? ctl->mptr[mat] : static_cast<const uint8_t *>(p.w_ptrs[mat]));

@@ -601,11 +601,15 @@ def _moe_q8_sub(q, lib, h, torch, stream, tables, scales, x, in_f, n_ff, n_used,
     def gemv(tb):
         return lib.qmm_moe_gemv_q8(h, q.NVFP4, tb.data_ptr(), scales.data_ptr(), qd.data_ptr(), dd.data_ptr(),
                                    y.data_ptr(), in_f, n_ff, n_used, 1, sptr)
-    if quant() != 0 or gemv(tables[0]) != 0:
-        raise RuntimeError("qmm_quantize_q8_1 / qmm_moe_gemv_q8 refused the call")
+    def fused(tb):
+        return lib.qmm_moe_gemv_q8_fused(h, q.NVFP4, tb.data_ptr(), scales.data_ptr(), x.data_ptr(), y.data_ptr(),
+                                         in_f, n_ff, n_used, 1, sptr)
+    if quant() != 0 or gemv(tables[0]) != 0 or fused(tables[0]) != 0:
+        raise RuntimeError("qmm_quantize_q8_1 / qmm_moe_gemv_q8 / qmm_moe_gemv_q8_fused refused the call")
     res = {}
     for label, calls, launches in (
             ("with_quantize", [(lambda tb=tb: quant() or gemv(tb)) for tb in tables], 2),
+            ("fused", [(lambda tb=tb: fused(tb)) for tb in tables], 1),
             ("kernel_only", [(lambda tb=tb: gemv(tb)) for tb in tables], 1)):
         ms, lo, hi = _time_calls(torch, stream, calls, 40)
         wg, wf = _rate(wbytes, ms, hbm_gbs)
@@ -720,13 +724,21 @@ def run_sub_benches(q, lib, h, torch, synth, stream, hbm_gbs):
             return st or lib.qmm_moe_down_q8(h, q.NVFP4, tb.data_ptr(), scales.data_ptr(), qd.data_ptr(),
                                              dd.data_ptr(), yd.data_ptr(), n_ff_d, gin, n_used, 1, ws.data_ptr(),
                                              wsb, sptr)
+        def down_q8_fused(tb):
+            return lib.qmm_moe_down_q8_fused(h, q.NVFP4, tb.data_ptr(), scales.data_ptr(), hact.data_ptr(),
+                                             yd.data_ptr(), n_ff_d, gin, n_used, 1, ws.data_ptr(), wsb, sptr)
         calls = [(lambda tb=tb: down_q8(tb)) for tb in tables]
-        if calls[0]() != 0:
-            raise RuntimeError("qmm_moe_down_q8 refused the call")
+        if calls[0]() != 0 or down_q8_fused(tables[0]) != 0:
+            raise RuntimeError("qmm_moe_down_q8 / qmm_moe_down_q8_fused refused the call")
         ms, lo, hi = _time_calls(torch, stream, calls, 48)
         wg, wf = _rate(wbytes, ms, hbm_gbs)
         out["moe_down_q8"] = {"us": round(ms * 1e3, 3), "us_min": round(lo * 1e3, 3), "us_max": round(hi * 1e3, 3),
                               "weight_bytes": wbytes, "weight_gbs": wg, "frac_hbm": wf, "launches_per_call": 3}
+        ms, lo, hi = _time_calls(torch, stream, [(lambda tb=tb: down_q8_fused(tb)) for tb in tables], 48)
+        wg, wf = _rate(wbytes, ms, hbm_gbs)
+        out["moe_down_q8"]["fused"] = {"us": round(ms * 1e3, 3), "us_min": round(lo * 1e3, 3),
+                                       "us_max": round(hi * 1e3, 3), "weight_gbs": wg, "frac_hbm": wf,
+                                       "launches_per_call": 2}
     except Exception as exc:
         out["moe_down_q8"] = {"error": f"{type(exc).__name__}: {exc}"}
     del keep, tables

@@ -7,7 +7,7 @@ loaded, importing the functions raises.
 
 Names follow the C ABI: ``qmm_create``, ``qmm_destroy``, ``qmm_gemm``,
 ``qmm_gemv``, ``qmm_moe_gemv``, ``qmm_moe_down``, ``qmm_quantize_q8_1``, ``qmm_moe_gemv_q8``,
-``qmm_moe_down_q8``, ``qmm_quantize_nvfp4``, ``qmm_gemm_fp4``, ``qmm_nvfp4_repack_v2``, ``qmm_dequant``, ``qmm_sync_status``,
+``qmm_moe_down_q8``, ``qmm_moe_gemv_q8_fused``, ``qmm_moe_down_q8_fused``, ``qmm_quantize_nvfp4``, ``qmm_gemm_fp4``, ``qmm_nvfp4_repack_v2``, ``qmm_dequant``, ``qmm_sync_status``,
 ``qmm_row_bytes``, ``qmm_gemm_workspace_bytes``, ``qmm_moe_down_workspace_bytes``,
 ``qmm_strerror``.
 """
@@ -32,7 +32,8 @@ STATUS = {0: "QMM_OK", 1: "QMM_ERR_INVALID_ARG", 2: "QMM_ERR_UNSUPPORTED", 3: "Q
 EXPORTS = ("qmm_create", "qmm_destroy", "qmm_strerror", "qmm_block_weights", "qmm_block_bytes",
            "qmm_row_bytes", "qmm_gemm_workspace_bytes", "qmm_gemm", "qmm_gemv", "qmm_moe_gemv",
            "qmm_moe_down_workspace_bytes", "qmm_moe_down", "qmm_nvfp4_repack_v2", "qmm_quantize_q8_1",
-           "qmm_moe_gemv_q8", "qmm_moe_down_q8", "qmm_quantize_nvfp4", "qmm_gemm_fp4",
+           "qmm_moe_gemv_q8", "qmm_moe_down_q8", "qmm_moe_gemv_q8_fused", "qmm_moe_down_q8_fused",
+           "qmm_quantize_nvfp4", "qmm_gemm_fp4",
            "qmm_dequant", "qmm_sync_status", "qmm_gemm_noalloc", "qmm_gemm_noalloc_status",
            "qmm_testing_set_wait_limit_ns",
            "qmm_testing_skip_first_stage_load")
@@ -78,6 +79,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         "qmm_gemm_fp4": (I, [P, P, P, P, I64, I64, I64, P]),
         "qmm_moe_gemv_q8": (I, [P, I, P, P, P, P, P, I64, I64, I, I, P]),
         "qmm_moe_down_q8": (I, [P, I, P, P, P, P, P, I64, I64, I, I, P, SZ, P]),
+        "qmm_moe_gemv_q8_fused": (I, [P, I, P, P, P, P, I64, I64, I, I, P]),
+        "qmm_moe_down_q8_fused": (I, [P, I, P, P, P, P, I64, I64, I, I, P, SZ, P]),
         "qmm_nvfp4_repack_v2": (I, [P, P, P, I64, I64, P]),
         "qmm_sync_status": (I, [P, P]),
         "qmm_gemm_noalloc": (I, [I, P, P, P, I64, I64, I64, P]),
@@ -206,6 +209,20 @@ def qmm_moe_down_q8(h, t, w_ptrs, scales, q, d, y, n_ff, gin, n_used, t_tokens, 
     _check(load().qmm_moe_down_q8(h, _dt(t), _ptr(w_ptrs), _ptr(scales), _ptr(q), _ptr(d), _ptr(y), n_ff, gin,
                                   n_used, t_tokens, _ptr(workspace), workspace_bytes, _stream(stream)),
            "qmm_moe_down_q8")
+
+
+def qmm_moe_gemv_q8_fused(h, t, w_ptrs, scales, x, y, in_f, n_ff, n_used, t_tokens, stream=None) -> None:
+    _check(load().qmm_moe_gemv_q8_fused(h, _dt(t), _ptr(w_ptrs), _ptr(scales), _ptr(x), _ptr(y), in_f, n_ff,
+                                        n_used, t_tokens, _stream(stream)), "qmm_moe_gemv_q8_fused")
+
+
+def qmm_moe_down_q8_fused(h, t, w_ptrs, scales, x, y, n_ff, gin, n_used, t_tokens, workspace=None,
+                          workspace_bytes=None, stream=None) -> None:
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None or isinstance(workspace, int) else workspace.numel() * workspace.element_size()
+    _check(load().qmm_moe_down_q8_fused(h, _dt(t), _ptr(w_ptrs), _ptr(scales), _ptr(x), _ptr(y), n_ff, gin,
+                                        n_used, t_tokens, _ptr(workspace), workspace_bytes, _stream(stream)),
+           "qmm_moe_down_q8_fused")
 
 
 def qmm_quantize_nvfp4(h, x, xq, rows, k, stream=None) -> None:

@@ -299,49 +299,91 @@ int qmm_moe_gemv_q8(qmm_handle h, qmm_dtype t, const void *const *w_ptrs, const 
         return QMM_ERR_OVERLAP;
     const int64_t rb = qmm_row_bytes(t, in_f);
     return on_device(h, [&] {
-        return qmm::launch_moe_q8(t, w_ptrs, rb, scales, q, d, y, in_f, n_ff, 2 * n_pairs, n_pairs, n_used,
+        return qmm::launch_moe_q8(t, w_ptrs, rb, scales, q, d, nullptr, y, in_f, n_ff, 2 * n_pairs, n_pairs, n_used,
                                   h->num_sms, h->d_status, h->wait_limit_ns, static_cast<cudaStream_t>(stream));
     });
 }
 
-int qmm_moe_down_q8(qmm_handle h, qmm_dtype t, const void *const *w_ptrs, const float *scales, const int8_t *q,
-                    const float *d, float *y, int64_t n_ff, int64_t gin, int n_used, int t_tokens, void *workspace,
-                    size_t workspace_bytes, void *stream) {
-    if (!valid_handle(h) || !known_dtype(t) || !w_ptrs || !scales || !q || !d || !y) return QMM_ERR_INVALID_ARG;
+int qmm_moe_gemv_q8_fused(qmm_handle h, qmm_dtype t, const void *const *w_ptrs, const float *scales, const float *x,
+                          float *y, int64_t in_f, int64_t n_ff, int n_used, int t_tokens, void *stream) {
+    if (!valid_handle(h) || !known_dtype(t) || !w_ptrs || !scales || !x || !y) return QMM_ERR_INVALID_ARG;
+    if (t != QMM_NVFP4 && t != QMM_NVFP4_V2) return QMM_ERR_UNSUPPORTED;
+    if (n_used < 1 || t_tokens < 1 || static_cast<int64_t>(n_used) * t_tokens > 4096) return QMM_ERR_SHAPE;
+    if (n_ff < 1 || n_ff > kMaxMN || in_f < 64 || in_f > QMM_Q8_MAX_K || in_f % 64 != 0) return QMM_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(w_ptrs) & 7u) != 0 || (reinterpret_cast<uintptr_t>(scales) & 3u) != 0 ||
+        !aligned16(x) || !aligned16(y))
+        return QMM_ERR_ALIGN;
+    const int n_pairs = n_used * t_tokens;
+    const size_t ybytes = static_cast<size_t>(2) * n_pairs * n_ff * sizeof(float);
+    if (overlaps(y, ybytes, x, static_cast<size_t>(t_tokens) * in_f * sizeof(float)) ||
+        overlaps(y, ybytes, scales, static_cast<size_t>(2) * n_pairs * sizeof(float)) ||
+        overlaps(y, ybytes, w_ptrs, static_cast<size_t>(2) * n_pairs * sizeof(void *)))
+        return QMM_ERR_OVERLAP;
+    const int64_t rb = qmm_row_bytes(t, in_f);
+    return on_device(h, [&] {
+        return qmm::launch_moe_q8(t, w_ptrs, rb, scales, nullptr, nullptr, x, y, in_f, n_ff, 2 * n_pairs, n_pairs,
+                                  n_used, h->num_sms, h->d_status, h->wait_limit_ns, static_cast<cudaStream_t>(stream));
+    });
+}
+
+// The down projection on Q8_1 activations: given as (q, d), or as x float32
+// quantized inside the kernel (q = d = NULL).
+static int moe_down_q8_impl(qmm_handle h, qmm_dtype t, const void *const *w_ptrs, const float *scales,
+                            const int8_t *q, const float *d, const float *x, float *y, int64_t n_ff, int64_t gin,
+                            int n_used, int t_tokens, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!valid_handle(h) || !known_dtype(t) || !w_ptrs || !scales || !y || (x ? (q || d) : (!q || !d)))
+        return QMM_ERR_INVALID_ARG;
     if (t != QMM_NVFP4 && t != QMM_NVFP4_V2) return QMM_ERR_UNSUPPORTED;
     if (n_used < 1 || t_tokens < 1 || static_cast<int64_t>(n_used) * t_tokens > 4096) return QMM_ERR_SHAPE;
     if (gin < 1 || gin > kMaxMN || n_ff < 64 || n_ff > QMM_Q8_MAX_K || n_ff % 64 != 0) return QMM_ERR_SHAPE;
     if ((reinterpret_cast<uintptr_t>(w_ptrs) & 7u) != 0 || (reinterpret_cast<uintptr_t>(scales) & 3u) != 0 ||
-        !aligned16(q) || !aligned16(d) || !aligned16(y))
+        (x ? !aligned16(x) : (!aligned16(q) || !aligned16(d))) || !aligned16(y))
         return QMM_ERR_ALIGN;
     const int n_pairs = n_used * t_tokens;
     const size_t ybytes = static_cast<size_t>(t_tokens) * gin * sizeof(float);
-    const size_t qbytes = static_cast<size_t>(n_pairs) * n_ff;
-    const size_t dbytes = static_cast<size_t>(n_pairs) * (n_ff / 32) * sizeof(float);
+    const size_t qbytes = x ? 0 : static_cast<size_t>(n_pairs) * n_ff;
+    const size_t dbytes = x ? 0 : static_cast<size_t>(n_pairs) * (n_ff / 32) * sizeof(float);
+    const size_t xbytes = x ? static_cast<size_t>(n_pairs) * n_ff * sizeof(float) : 0;
     const size_t sbytes = static_cast<size_t>(n_pairs) * sizeof(float);
     const size_t pbytes = static_cast<size_t>(n_pairs) * sizeof(void *);
-    if (overlaps(y, ybytes, q, qbytes) || overlaps(y, ybytes, d, dbytes) || overlaps(y, ybytes, scales, sbytes) ||
-        overlaps(y, ybytes, w_ptrs, pbytes))
+    if (overlaps(y, ybytes, q, qbytes) || overlaps(y, ybytes, d, dbytes) || overlaps(y, ybytes, x, xbytes) ||
+        overlaps(y, ybytes, scales, sbytes) || overlaps(y, ybytes, w_ptrs, pbytes))
         return QMM_ERR_OVERLAP;
     const size_t need = qmm_moe_down_workspace_bytes(gin, n_used, t_tokens);
     if (need) {
         if (!workspace || workspace_bytes < need) return QMM_ERR_WORKSPACE;
         if (!aligned16(workspace)) return QMM_ERR_ALIGN;
         if (overlaps(workspace, need, y, ybytes) || overlaps(workspace, need, q, qbytes) ||
-            overlaps(workspace, need, d, dbytes) || overlaps(workspace, need, scales, sbytes) ||
-            overlaps(workspace, need, w_ptrs, pbytes))
+            overlaps(workspace, need, d, dbytes) || overlaps(workspace, need, x, xbytes) ||
+            overlaps(workspace, need, scales, sbytes) || overlaps(workspace, need, w_ptrs, pbytes))
             return QMM_ERR_OVERLAP;
     }
     const int64_t rb = qmm_row_bytes(t, n_ff);
     return on_device(h, [&]() -> cudaError_t {
         // the pair products (activation row = pair), then the per-token combine
         float *part = n_used == 1 ? y : static_cast<float *>(workspace);
-        cudaError_t e = qmm::launch_moe_q8(t, w_ptrs, rb, scales, q, d, part, n_ff, gin, n_pairs, n_pairs, 1,
+        cudaError_t e = qmm::launch_moe_q8(t, w_ptrs, rb, scales, q, d, x, part, n_ff, gin, n_pairs, n_pairs, 1,
                                            h->num_sms, h->d_status, h->wait_limit_ns,
                                            static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess || n_used == 1) return e;
         return qmm::launch_moe_combine(part, y, gin, n_used, t_tokens, h->num_sms, static_cast<cudaStream_t>(stream));
     });
+}
+
+int qmm_moe_down_q8(qmm_handle h, qmm_dtype t, const void *const *w_ptrs, const float *scales, const int8_t *q,
+                    const float *d, float *y, int64_t n_ff, int64_t gin, int n_used, int t_tokens, void *workspace,
+                    size_t workspace_bytes, void *stream) {
+    if (!q || !d) return QMM_ERR_INVALID_ARG;
+    return moe_down_q8_impl(h, t, w_ptrs, scales, q, d, nullptr, y, n_ff, gin, n_used, t_tokens, workspace,
+                            workspace_bytes, stream);
+}
+
+int qmm_moe_down_q8_fused(qmm_handle h, qmm_dtype t, const void *const *w_ptrs, const float *scales, const float *x,
+                          float *y, int64_t n_ff, int64_t gin, int n_used, int t_tokens, void *workspace,
+                          size_t workspace_bytes, void *stream) {
+    if (!x) return QMM_ERR_INVALID_ARG;
+    return moe_down_q8_impl(h, t, w_ptrs, scales, nullptr, nullptr, x, y, n_ff, gin, n_used, t_tokens, workspace,
+                            workspace_bytes, stream);
 }
 
 int qmm_quantize_nvfp4(qmm_handle h, const float *x, void *xq, int64_t rows, int64_t k, void *stream) {

@@ -47,9 +47,11 @@ cudaError_t launch_quantize_q8_1(const float *x, int8_t *q, float *d, int64_t ro
 // dst[mat][r] = scales[mat] * sum_c W_mat[r][c] * q[a][c] * d[a][c/32] with
 // activation row a = (mat % n_pairs) / n_used, for mats matrices of
 // rows_per_mat rows; k % 64 == 0, k <= QMM_Q8_MAX_K.
+// With x non-null the kernel quantizes the activation rows x [act rows][k]
+// float32 itself (the same bytes launch_quantize_q8_1 writes; q, d unused).
 cudaError_t launch_moe_q8(int dtype, const void *const *w_ptrs, int64_t rb, const float *scales, const int8_t *q,
-                          const float *d, float *dst, int64_t k, int64_t rows_per_mat, int mats, int n_pairs,
-                          int n_used, int num_sms, uint32_t *status, uint64_t limit_ns, cudaStream_t st);
+                          const float *d, const float *x, float *dst, int64_t k, int64_t rows_per_mat, int mats,
+                          int n_pairs, int n_used, int num_sms, uint32_t *status, uint64_t limit_ns, cudaStream_t st);
 
 // Activation rows [rows][k] f32 -> NVFP4 V2 rows (E2M1 codes, one E4M3 scale
 // per 16, nearest values, decided in float32); k % 256 == 0.

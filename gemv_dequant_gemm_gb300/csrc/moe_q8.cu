@@ -26,8 +26,12 @@
 // takes row w of every stage of its CTA.  Lane l owns the 64-weight groups
 // l, l+32, ... of the row (J of them), and keeps the matching activation
 // bytes, block scales and offset terms in registers for as long as the
-// activation row stays the same.  Every wait is bounded; a stage with a NULL
-// or misaligned matrix pointer is skipped, reported, and its rows set to NaN.
+// activation row stays the same.  Given the float32 activation instead of
+// its Q8_1 blocks, the compute warps quantize each new activation row
+// together into a small shared-memory table first (the quantizer kernel's
+// steps, so the same bytes), and the lanes read their groups from there.
+// Every wait is bounded; a stage with a NULL or misaligned matrix pointer is
+// skipped, reported, and its rows set to NaN.
 #include <cuda_fp8.h>
 
 #include <algorithm>
@@ -49,6 +53,7 @@ struct Params {
     const float *scales;
     const int8_t *q;  // [act rows][k]
     const float *d;   // [act rows][k/32]
+    const float *x;   // [act rows][k] float32, quantized in the kernel (q, d unused) when not null
     float *dst;       // [mats][rows_per_mat]
     int64_t k, rb;
     int rows_per_mat, mats, n_pairs, n_used;
@@ -108,6 +113,56 @@ __device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float (&s)[4]) {
     s[3] = b.y;
 }
 
+// Q8_1 arithmetic shared by the quantizer kernel and the kernels that
+// quantize their activation themselves: d = amax/127, the reciprocal, and a
+// code, each one float32 operation, so both produce the same bytes.
+__device__ __forceinline__ float q8_block_scale(float amax) { return __fdiv_rn(amax, 127.0f); }
+__device__ __forceinline__ float q8_block_inv(float d) { return d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f; }
+__device__ __forceinline__ int q8_code(float v, float id) { return static_cast<int>(roundf(__fmul_rn(v, id))); }
+
+// A float32 activation row of k values (k % 64 == 0, 16-byte aligned) as
+// Q8_1 into shared memory, by the CTA's NT compute threads together: codes
+// [k/64][16] words (value 4i+j of a 64-value group in byte j of word i), then
+// block scales [k/64][2].  Thread i takes values 8i .. 8i+7; the four threads
+// of a 32-value block meet in a shuffle for its amax.  Every thread of the
+// NT calls it (the shuffles need whole warps).
+template <int NT>
+__device__ __forceinline__ void q8_quantize_row_shared(const float *xr, int64_t k, uint32_t *tq, float *td, int ct) {
+    const int n8 = static_cast<int>(k >> 3);
+    for (int base = ct & ~31; base < n8; base += NT) {
+        const int i = base + (ct & 31);
+        const bool ok = i < n8;
+        float v[8];
+        if (ok) {
+            const float4 a = __ldg(reinterpret_cast<const float4 *>(xr) + 2 * i);
+            const float4 c = __ldg(reinterpret_cast<const float4 *>(xr) + 2 * i + 1);
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+            v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
+        } else {
+#pragma unroll
+            for (int t = 0; t < 8; ++t) v[t] = 0.0f;
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) amax = fmaxf(amax, fabsf(v[t]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+        if (ok) {
+            const float db = q8_block_scale(amax);
+            const float id = q8_block_inv(db);
+#pragma unroll
+            for (int w = 0; w < 2; ++w) {
+                uint32_t word = 0;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    word |= (static_cast<uint32_t>(q8_code(v[4 * w + j], id)) & 0xFFu) << (8 * j);
+                tq[2 * i + w] = word;  // group i/8, words 2(i%8), 2(i%8)+1
+            }
+            if ((i & 3) == 0) td[i >> 2] = db;  // block i/4 = group i/8, half (i/4)%2
+        }
+    }
+}
+
 // Four codes against four activation bytes: the positive lookup (negative
 // codes give 0) and the lookup on the sign-flipped selector (positive codes
 // give 0) each feed one dp4a, which is the dp4a of their OR.
@@ -127,13 +182,16 @@ __device__ __forceinline__ int region_dot(uint32_t c0, uint32_t c1, const uint32
     return dot4(c1 >> 16, x1 >> 16, qw[3], v);
 }
 
-template <int F, int J, int RW>
+template <int F, int J, int RW, bool FX>
 __global__ void __launch_bounds__(mq::THREADS, 1) moe_q8_kernel(const mq::Params p) {
     using namespace mq;
     constexpr int SR = COMPUTE_WARPS * RW;  // rows per stage: warp w takes rows w*RW .. w*RW+RW-1
     extern __shared__ uint8_t smem_raw[];
     uint8_t *ring = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     Ctl *ctl = reinterpret_cast<Ctl *>(ring + p.ring * p.stage_bytes);
+    // the quantized activation row (FX): codes [k/64][16] words, then scales [k/64][2]
+    uint32_t *tq = reinterpret_cast<uint32_t *>((reinterpret_cast<uintptr_t>(ctl + 1) + 15) & ~uintptr_t(15));
+    float *td = reinterpret_cast<float *>(tq + 16 * (p.k >> 6));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -225,24 +283,46 @@ __global__ void __launch_bounds__(mq::THREADS, 1) moe_q8_kernel(const mq::Params
             cur_mat = mat;
             scale = 0.5f * (table ? ctl->mscale[mat] : __ldg(p.scales + mat));  // codes hold 2 * e2m1
             if (act != prev_act) {
+                if constexpr (FX) {
+                    // every compute warp has copied the previous row's table into
+                    // its registers; quantize the new row together, then read it
+                    asm volatile("bar.sync 1, %0;" ::"n"(32 * COMPUTE_WARPS) : "memory");
+                    q8_quantize_row_shared<32 * COMPUTE_WARPS>(p.x + static_cast<int64_t>(act) * p.k, p.k, tq, td,
+                                                               threadIdx.x);
+                    asm volatile("bar.sync 1, %0;" ::"n"(32 * COMPUTE_WARPS) : "memory");
+                }
 #pragma unroll
                 for (int jj = 0; jj < J; ++jj) {
                     const int u = lane + 32 * jj;
                     if (u < U) {
-                        const uint4 *src =
-                            reinterpret_cast<const uint4 *>(p.q + static_cast<int64_t>(act) * p.k) + 4 * u;
+                        if constexpr (FX) {
+                            const uint4 *src = reinterpret_cast<const uint4 *>(tq) + 4 * u;
 #pragma unroll
-                        for (int t = 0; t < 4; ++t) {
-                            const uint4 v = __ldg(src + t);
-                            qv[jj][4 * t] = v.x;
-                            qv[jj][4 * t + 1] = v.y;
-                            qv[jj][4 * t + 2] = v.z;
-                            qv[jj][4 * t + 3] = v.w;
+                            for (int t = 0; t < 4; ++t) {
+                                const uint4 v = src[t];
+                                qv[jj][4 * t] = v.x;
+                                qv[jj][4 * t + 1] = v.y;
+                                qv[jj][4 * t + 2] = v.z;
+                                qv[jj][4 * t + 3] = v.w;
+                            }
+                            dd[jj][0] = td[2 * u];
+                            dd[jj][1] = td[2 * u + 1];
+                        } else {
+                            const uint4 *src =
+                                reinterpret_cast<const uint4 *>(p.q + static_cast<int64_t>(act) * p.k) + 4 * u;
+#pragma unroll
+                            for (int t = 0; t < 4; ++t) {
+                                const uint4 v = __ldg(src + t);
+                                qv[jj][4 * t] = v.x;
+                                qv[jj][4 * t + 1] = v.y;
+                                qv[jj][4 * t + 2] = v.z;
+                                qv[jj][4 * t + 3] = v.w;
+                            }
+                            const float2 ds = __ldg(
+                                reinterpret_cast<const float2 *>(p.d + static_cast<int64_t>(act) * (p.k >> 5)) + u);
+                            dd[jj][0] = ds.x;
+                            dd[jj][1] = ds.y;
                         }
-                        const float2 ds =
-                            __ldg(reinterpret_cast<const float2 *>(p.d + static_cast<int64_t>(act) * (p.k >> 5)) + u);
-                        dd[jj][0] = ds.x;
-                        dd[jj][1] = ds.y;
 #pragma unroll
                         for (int r = 0; r < 4; ++r) {
                             int sum = 0;
@@ -352,9 +432,9 @@ __global__ void __launch_bounds__(256) quantize_q8_1_kernel(const float *__restr
         float a = fabsf(v);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
-        const float db = __fdiv_rn(a, 127.0f);
-        const float id = db != 0.0f ? __fdiv_rn(1.0f, db) : 0.0f;
-        q[b * 32 + lane] = static_cast<int8_t>(roundf(__fmul_rn(v, id)));
+        const float db = q8_block_scale(a);
+        const float id = q8_block_inv(db);
+        q[b * 32 + lane] = static_cast<int8_t>(q8_code(v, id));
         if (lane == 0) d[b] = db;
     }
 }
@@ -367,29 +447,35 @@ cudaError_t launch_quantize_q8_1(const float *x, int8_t *q, float *d, int64_t ro
     return launch_pdl(quantize_q8_1_kernel, dim3(grid), dim3(256), 0, st, dim3(1, 1, 1), x, q, d, nblocks);
 }
 
-template <int F, int J, int RW> static cudaError_t launch_q8_j(const mq::Params &p, int num_sms, cudaStream_t st) {
+template <int F, int J, int RW, bool FX>
+static cudaError_t launch_q8_j(const mq::Params &p, int num_sms, cudaStream_t st) {
     using namespace mq;
-    const size_t smem = 128 + static_cast<size_t>(p.ring) * p.stage_bytes + sizeof(Ctl) + 16;
-    cudaError_t e = cudaFuncSetAttribute(moe_q8_kernel<F, J, RW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const size_t smem = 128 + static_cast<size_t>(p.ring) * p.stage_bytes + sizeof(Ctl) + 16 +
+                        (FX ? static_cast<size_t>(p.k / 64) * 72 : 0);
+    cudaError_t e = cudaFuncSetAttribute(moe_q8_kernel<F, J, RW, FX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int grid = std::min(p.total_stages, num_sms);
-    return launch_pdl(moe_q8_kernel<F, J, RW>, dim3(grid), dim3(THREADS), smem, st, dim3(1, 1, 1), p);
+    return launch_pdl(moe_q8_kernel<F, J, RW, FX>, dim3(grid), dim3(THREADS), smem, st, dim3(1, 1, 1), p);
 }
 
-template <int F, int RW> static cudaError_t launch_q8_f(const mq::Params &p, int num_sms, cudaStream_t st) {
+template <int F, int RW, bool FX> static cudaError_t launch_q8_fx(const mq::Params &p, int num_sms, cudaStream_t st) {
     switch ((p.k / 64 + 31) / 32) {
-    case 1: return launch_q8_j<F, 1, RW>(p, num_sms, st);
-    case 2: return launch_q8_j<F, 2, RW>(p, num_sms, st);
-    case 3: return launch_q8_j<F, 3, RW>(p, num_sms, st);
-    case 4: return launch_q8_j<F, 4, RW>(p, num_sms, st);
+    case 1: return launch_q8_j<F, 1, RW, FX>(p, num_sms, st);
+    case 2: return launch_q8_j<F, 2, RW, FX>(p, num_sms, st);
+    case 3: return launch_q8_j<F, 3, RW, FX>(p, num_sms, st);
+    case 4: return launch_q8_j<F, 4, RW, FX>(p, num_sms, st);
     default: return cudaErrorInvalidValue;
     }
 }
 
+template <int F, int RW> static cudaError_t launch_q8_f(const mq::Params &p, int num_sms, cudaStream_t st) {
+    return p.x ? launch_q8_fx<F, RW, true>(p, num_sms, st) : launch_q8_fx<F, RW, false>(p, num_sms, st);
+}
+
 cudaError_t launch_moe_q8(int dtype, const void *const *w_ptrs, int64_t rb, const float *scales, const int8_t *q,
-                          const float *d, float *dst, int64_t k, int64_t rows_per_mat, int mats, int n_pairs,
-                          int n_used, int num_sms, uint32_t *status, uint64_t limit_ns, cudaStream_t st) {
+                          const float *d, const float *x, float *dst, int64_t k, int64_t rows_per_mat, int mats,
+                          int n_pairs, int n_used, int num_sms, uint32_t *status, uint64_t limit_ns, cudaStream_t st) {
     using namespace mq;
     if (k % 64 != 0 || k > QMM_Q8_MAX_K || rb % 4 != 0) return cudaErrorInvalidValue;
     Params p = {};
@@ -397,6 +483,7 @@ cudaError_t launch_moe_q8(int dtype, const void *const *w_ptrs, int64_t rb, cons
     p.scales = scales;
     p.q = q;
     p.d = d;
+    p.x = x;
     p.dst = dst;
     p.k = k;
     p.rb = rb;
@@ -406,7 +493,7 @@ cudaError_t launch_moe_q8(int dtype, const void *const *w_ptrs, int64_t rb, cons
     p.n_used = n_used;
     // two rows per warp and stage when three such stages fit in shared memory
     // (more independent work per warp, half the per-row overhead), else one
-    const int64_t budget = SMEM_BUDGET - static_cast<int64_t>(sizeof(Ctl)) - 256;
+    const int64_t budget = SMEM_BUDGET - static_cast<int64_t>(sizeof(Ctl)) - 256 - (x ? k / 64 * 72 : 0);
     const int rw = (budget / ((2 * COMPUTE_WARPS * rb + 15) / 16 * 16) >= 3) ? 2 : 1;
     const int sr = COMPUTE_WARPS * rw;
     p.stages_per_mat = static_cast<int>((rows_per_mat + sr - 1) / sr);

@@ -257,6 +257,22 @@ int qmm_moe_down_q8(qmm_handle h, qmm_dtype t, const void *const *w_ptrs, const 
                     const int8_t *q, const float *d, float *y, int64_t n_ff, int64_t gin, int n_used,
                     int t_tokens, void *workspace, size_t workspace_bytes, void *stream);
 
+/* The two calls above with the quantization inside the product kernel: x is
+ * the float32 activation (qmm_moe_gemv_q8_fused: [t_tokens][in_f], one row
+ * per token; qmm_moe_down_q8_fused: [n_pairs][n_ff], one row per pair),
+ * 16-byte aligned, overlapping neither y nor the workspace.  Each CTA turns
+ * the activation values its lanes multiply into Q8_1 codes and block scales
+ * with the steps of qmm_quantize_q8_1, so y is bit-identical to
+ * qmm_quantize_q8_1 followed by qmm_moe_gemv_q8 / qmm_moe_down_q8 on the same
+ * x; one kernel launch fewer, and no q, d buffers.  Other arguments, limits,
+ * accuracy and errors as those calls. */
+int qmm_moe_gemv_q8_fused(qmm_handle h, qmm_dtype t, const void *const *w_ptrs, const float *scales,
+                          const float *x, float *y, int64_t in_f, int64_t n_ff, int n_used, int t_tokens,
+                          void *stream);
+int qmm_moe_down_q8_fused(qmm_handle h, qmm_dtype t, const void *const *w_ptrs, const float *scales,
+                          const float *x, float *y, int64_t n_ff, int64_t gin, int n_used, int t_tokens,
+                          void *workspace, size_t workspace_bytes, void *stream);
+
 /* Activation rows for the block-scaled FP4 product (qmm_gemm_fp4): x
  * [rows][k] float32 becomes NVFP4 V2 rows xq (rows * qmm_row_bytes(
  * QMM_NVFP4_V2, k) bytes: k/2 code bytes, element 2j in the low nibble of

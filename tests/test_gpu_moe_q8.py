@@ -4,7 +4,8 @@ qmm_quantize_q8_1 must reproduce the oracle's integer codes and block scales
 bit for bit (both decide them in float32 by the same steps).  qmm_moe_gemv_q8
 and qmm_moe_down_q8 must be within 1e-5 * sum|W * q*d| of the exact products
 on the quantized activation (oracle.moe_gate_up_q8 / moe_down_q8), for the
-36-byte NVFP4 groups and the V2 rows.
+36-byte NVFP4 groups and the V2 rows.  The fused calls, which quantize inside
+the product kernel, must equal the two-call path bit for bit.
 """
 import numpy as np
 import pytest
@@ -231,3 +232,91 @@ def test_moe_down_q8_tokens(h, n_used, t):
     qo, do = oracle.quantize_q8_1(hact, n_pairs, n_ff)
     ref, am = oracle.moe_down_q8("nvfp4", mats, scales, qo, do, n_ff, gin, n_used, t)
     assert_close(y, ref, am, FMA_REL, what=f"n_used={n_used} t={t}")
+
+
+# ---- the fused calls (quantization inside the product kernel) --------------------
+
+def _table(mats):
+    dm = [dev(a) for a in mats]
+    return dm, torch.tensor([a.data_ptr() for a in dm], dtype=torch.int64, device="cuda")
+
+
+@pytest.mark.parametrize("fmt,in_f,n_ff,n_used,t", [("nvfp4", 4096, 2048, 8, 1), ("nvfp4_v2", 4096, 2048, 8, 1),
+                                                     ("nvfp4", 192, 37, 3, 2), ("nvfp4_v2", 8192, 21, 1, 3),
+                                                     ("nvfp4", 64, 16, 2, 1)])
+def test_moe_gate_up_q8_fused_equals_quantize_then_product(h, fmt, in_f, n_ff, n_used, t):
+    # the served shape and ragged ones (idle lanes, one to four groups per
+    # lane, several tokens): bit-identical to the two calls, and within the
+    # tolerance of the oracle on the oracle's own quantization
+    n_pairs = n_used * t
+    mats = [synth.nvfp4_rows(synth.nvfp4_matrix_seed(5, j, p), n_ff, in_f) for p in range(2) for j in range(n_pairs)]
+    mats = _as_fmt(fmt, mats, n_ff, in_f)
+    scales = _scales(2 * n_pairs)
+    x = synth.activations(t, in_f, seed=21)
+    x[0, :32] *= 40.0  # one block with a large scale
+    x[-1, 64:96] = 0.0  # one all-zero block (d = 0)
+    qd, dd = _quantize(h, x, t, in_f)
+    st, y2 = _run_gate_up(h, fmt, mats, scales, qd, dd, in_f, n_ff, n_used, t)
+    assert st == 0
+    _, table = _table(mats)
+    y1 = nan_filled(2, n_pairs, n_ff)
+    q.qmm_moe_gemv_q8_fused(h, fmt, table, dev(scales), dev(x), y1, in_f, n_ff, n_used, t)
+    assert q.qmm_sync_status(h) == 0
+    y1 = y1.cpu().numpy()
+    assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
+    qo, do = oracle.quantize_q8_1(x, t, in_f)
+    ref, am = oracle.moe_gate_up_q8(fmt, mats, scales, qo, do, in_f, n_ff, n_used, t)
+    assert_close(y1, ref, am, FMA_REL, what=f"fused {fmt} in_f={in_f}")
+
+
+@pytest.mark.parametrize("fmt,n_ff,gin,n_used,t", [("nvfp4", 2048, 4096, 8, 1), ("nvfp4_v2", 2048, 4096, 8, 1),
+                                                    ("nvfp4", 320, 53, 3, 2), ("nvfp4", 128, 40, 1, 3)])
+def test_moe_down_q8_fused_equals_quantize_then_product(h, fmt, n_ff, gin, n_used, t):
+    n_pairs = n_used * t
+    mats = _as_fmt(fmt, [synth.nvfp4_rows(synth.nvfp4_matrix_seed(6, j, 2), gin, n_ff) for j in range(n_pairs)],
+                   gin, n_ff)
+    scales = _scales(n_pairs)
+    hact = synth.activations(n_pairs, n_ff, seed=H_SEED + 1)
+    qd, dd = _quantize(h, hact, n_pairs, n_ff)
+    st, y2 = _run_down(h, fmt, mats, scales, qd, dd, n_ff, gin, n_used, t)
+    assert st == 0
+    _, table = _table(mats)
+    y1 = nan_filled(t, gin)
+    wsb = q.qmm_moe_down_workspace_bytes(gin, n_used, t)
+    ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda") if wsb else None
+    q.qmm_moe_down_q8_fused(h, fmt, table, dev(scales), dev(hact), y1, n_ff, gin, n_used, t, ws, wsb)
+    assert q.qmm_sync_status(h) == 0
+    y1 = y1.cpu().numpy()
+    assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
+    qo, do = oracle.quantize_q8_1(hact, n_pairs, n_ff)
+    ref, am = oracle.moe_down_q8(fmt, mats, scales, qo, do, n_ff, gin, n_used, t)
+    assert_close(y1, ref, am, FMA_REL, what=f"fused down {fmt} n_used={n_used} t={t}")
+
+
+def test_q8_fused_argument_errors(h):
+    in_f, n_ff = 128, 16
+    mats = [dev(synth.nvfp4_rows(synth.nvfp4_matrix_seed(3, j, 0), n_ff, in_f)) for j in range(2)]
+    table = torch.tensor([a.data_ptr() for a in mats], dtype=torch.int64, device="cuda")
+    scales = dev(_scales(2))
+    x = dev(synth.activations(1, in_f))
+    y = nan_filled(2, 1, n_ff)
+    with pytest.raises(q.QmmError) as e:
+        q.qmm_moe_gemv_q8_fused(h, "q8_0", table, scales, x, y, in_f, n_ff, 1, 1)
+    assert e.value.status == 2  # NVFP4 only
+    with pytest.raises(q.QmmError) as e:
+        q.qmm_moe_gemv_q8_fused(h, "nvfp4", table, scales, x, y, 96, n_ff, 1, 1)
+    assert e.value.status == 3  # in_f % 64
+    with pytest.raises(q.QmmError) as e:
+        q.qmm_moe_gemv_q8_fused(h, "nvfp4", table, scales, x.data_ptr() + 4, y, in_f, n_ff, 1, 1)
+    assert e.value.status == 4  # x not 16-byte aligned
+    with pytest.raises(q.QmmError) as e:
+        q.qmm_moe_gemv_q8_fused(h, "nvfp4", table, scales, y, y, in_f, n_ff, 1, 1)
+    assert e.value.status == 9  # y overlaps x
+    yd = nan_filled(1, 40)
+    with pytest.raises(q.QmmError) as e:
+        q.qmm_moe_down_q8_fused(h, "nvfp4", table, scales, x, yd, 96, 40, 1, 1)
+    assert e.value.status == 3  # n_ff % 64
+    with pytest.raises(q.QmmError) as e:
+        q.qmm_moe_down_q8_fused(h, "nvfp4", table, scales, 0, yd, in_f, 40, 1, 1)
+    assert e.value.status == 1  # no activation
+    assert np.all(np.isnan(y.cpu().numpy())) and np.all(np.isnan(yd.cpu().numpy()))

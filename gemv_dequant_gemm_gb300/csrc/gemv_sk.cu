@@ -420,7 +420,11 @@ bool plan_sk(int qk, int bb, int64_t m, int64_t k, int nv, int nz, int jcap, int
             if (J > jmax) continue;
             if (tk < 64 && us >= 64) continue;  // at least two warps when the slice allows
             const int64_t waste = tk * J - us;
-            if (waste < best_waste || (waste == best_waste && tk > best_tk)) {
+            // among equal waste: with one activation row per CTA, more units
+            // per thread (more independent work for the same registers);
+            // with more, more threads (measured on GB300)
+            const bool better_tie = nv == 1 ? tk < best_tk : tk > best_tk;
+            if (waste < best_waste || (waste == best_waste && better_tie)) {
                 best_waste = waste;
                 best_tk = tk;
             }
@@ -435,7 +439,7 @@ bool plan_sk(int qk, int bb, int64_t m, int64_t k, int nv, int nz, int jcap, int
             pl.tk = best_tk;
             pl.J = static_cast<int>((us + best_tk - 1) / best_tk);
         }
-        if (warps >= static_cast<int64_t>(num_sms) * 12) break;  // the fewest splits that fill the GPU
+        if (warps >= static_cast<int64_t>(num_sms) * 8) break;  // the fewest splits that fill the GPU
     }
     if (!have) return false;
     // rows per CTA for about 16 resident warps per SM when a thread holds one

@@ -25,7 +25,7 @@
 //               the same in every lane quarter, four columns per MMA), one
 //               tcgen05.st of 16 columns per operand and warp; then the
 //               epilogue: tcgen05.ld of the fp32 accumulator into shared
-//               memory as [n][m], one TMA store of the tile (split-K: a
+//               memory as [n][m], a TMA store per 32 columns (split-K: a
 //               fixed-order sum of the cluster's partial tiles through
 //               distributed shared memory, no atomics).
 // Every wait is bounded; a wait that runs out latches the timeout bit and
@@ -77,7 +77,7 @@ struct Params {
     float *dst;
     int M, N, K;
     int splits;  // CTAs per output tile (a cluster along z), each a contiguous share of the k stages
-    int dtma;    // 1: the tile is stored with one TMA store through map_d (M % 4 == 0)
+    int dtma;    // 1: the tile is stored with TMA stores through map_d (M % 4 == 0)
     uint32_t *status;
     uint64_t limit_ns;
 };
@@ -231,7 +231,8 @@ __global__ void __launch_bounds__(f4::THREADS, 1)
 
     // ---------------- epilogue (warps 2-5) ----------------
     // The fp32 tile goes through shared memory as [BN][BM] (m contiguous; the
-    // stage ring is free once every MMA has completed), then one TMA store;
+    // stage ring is free once every MMA has completed), a TMA store for each
+    // 32 columns as soon as the four warps have written them;
     // with split-K the CTAs of a cluster each sum a column slice of all the
     // partial tiles in rank order through distributed shared memory.
     const bool is_epi = warp >= 2;
@@ -241,19 +242,29 @@ __global__ void __launch_bounds__(f4::THREADS, 1)
         if (warp == 2 && lane == 0) griddep_launch();
         if (!drained) *abort = 1;
         have = __all_sync(0xFFFFFFFFu, drained && !*abort);
-        if (have) {
-            tc_fence_after();
-            const int q = warp & 3;
-            const int r = 32 * q + lane;  // tile row (m)
+        if (have) tc_fence_after();
+        const int q = warp & 3;
+        const int r = 32 * q + lane;  // tile row (m)
+        const bool pipe = S == 1 && p.dtma;  // store each 32-column group as soon as it is in shared memory
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+        for (int c = 0; c < BN / 32; ++c) {
+            if (have) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + 32 * c, v);
                 tmem_ld_wait();
 #pragma unroll
                 for (int j2 = 0; j2 < 32; ++j2) sRed[(32 * c + j2) * BM + r] = __uint_as_float(v[j2]);
             }
+            if (pipe) {
+                fence_proxy_async_smem();
+                asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
+                if (warp == 2 && lane == 0 && !*abort) {
+                    tma_store_2d(&map_d, m0, n0 + 32 * c, sRed + 32 * c * BM);
+                    bulk_commit_group();
+                }
+            }
         }
+        if (pipe && warp == 2 && lane == 0 && !*abort) bulk_wait_group_read0();
     } else if (threadIdx.x == 0) {
         griddep_launch();
     }
@@ -262,11 +273,7 @@ __global__ void __launch_bounds__(f4::THREADS, 1)
             fence_proxy_async_smem();  // the generic-proxy writes above, before the TMA store reads them
             asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
             if (p.dtma) {
-                if (warp == 2 && lane == 0 && !*abort) {
-                    tma_store_2d(&map_d, m0, n0, sRed);
-                    bulk_commit_group();
-                    bulk_wait_group_read0();  // the source stays valid until the engine has read it
-                }
+                // stored group by group above
             } else if (!*abort) {
                 const int et = threadIdx.x - 64;  // 0..127
                 for (int it = et; it < BN * BM; it += 128) {
@@ -417,7 +424,7 @@ cudaError_t launch_gemm_fp4(const void *w, const void *xq, float *dst, int64_t m
         auto fn = f4_encode_fn();
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(m), static_cast<cuuint64_t>(n)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(m) * 4};
-        const cuuint32_t box[2] = {static_cast<cuuint32_t>(BM), static_cast<cuuint32_t>(BN)};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(BM), 32u};
         const cuuint32_t estr[2] = {1, 1};
         p.dtma = fn && fn(&mdst, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, dst, dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,

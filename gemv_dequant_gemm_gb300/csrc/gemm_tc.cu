@@ -33,7 +33,8 @@
 //               touch shared memory or HBM, so the shared-memory bandwidth is
 //               left to the X stream and the raw bytes; then the same warps
 //               run the epilogue: tcgen05.ld, the tile into shared memory as
-//               [n][m], one TMA store.
+//               [n][m], 32 columns at a time, each group leaving with a TMA
+//               store while the next is read out of tensor memory.
 //
 // Stages are long on purpose: the issuing thread waits on mbarriers between
 // stages, and a wait that follows tcgen05.commit costs a few hundred cycles,
@@ -159,7 +160,7 @@ struct GemmParams {
     int raw_g;   // rows per 16-byte-aligned row group of the raw-weight tensor map; 0 = per-row bulk copies
     int splits;  // CTAs per output tile (cluster size along z)
     int x3d;     // 1: X (and f32 W) maps are 3-D [k atoms][rows][atom]: one TMA request per stage
-    int dtma;    // 1: the tile is stored with one TMA store through tmap_d (m % 4 == 0)
+    int dtma;    // 1: the tile is stored with TMA stores through tmap_d (m % 4 == 0)
     uint32_t *status;
     uint64_t limit_ns;
     int debug_skip;
@@ -465,26 +466,32 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
     const uint32_t dcol = static_cast<uint32_t>((SUB == 2) ? BN * hh : (BN / 2) * hh);  // its TMEM column
     const int rloc = (SUB == 2 ? 128 * hh : 0) + 32 * q + lane;      // tile row of this thread
     if (S == 1 && p.dtma) {
-        // tile -> shared memory as [BN][ROWS] (m contiguous), then one TMA store
+        // tile -> shared memory as [BN][ROWS] (m contiguous), 32 columns at a
+        // time; each finished group of columns leaves with a TMA store while
+        // the next is read out of tensor memory
         if (is_epi) {
-            if (have) {
-                tc_fence_after();
+            if (have) tc_fence_after();
 #pragma unroll 1
-                for (int c = 0; c < ECOLS / 32; ++c) {
+            for (int c = 0; c < ECOLS / 32; ++c) {
+                if (have) {
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + dcol + 32 * c, v);
                     tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < 32; ++j) sRed[(colbase + 32 * c + j) * ROWS + rloc] = __uint_as_float(v[j]);
                 }
+                fence_proxy_async_smem();  // the generic-proxy writes above, before the async-proxy read
+                asm volatile("bar.sync 1, %0;" ::"r"(32 * NUM_DECODE_WARPS) : "memory");  // every epilogue warp
+                if (warp == WARP_DEC0 && lane == 0 && !*abort) {
+                    // columns 32c.. of each column half (SUB == 1) or of the tile (SUB == 2)
+                    for (int h2 = 0; h2 < (SUB == 2 ? 1 : 2); ++h2) {
+                        const int col = (SUB == 2 ? 0 : (BN / 2) * h2) + 32 * c;
+                        tma_store_2d(&tmap_d, m0, n0 + col, sRed + col * ROWS);
+                    }
+                    bulk_commit_group();
+                }
             }
-            fence_proxy_async_smem();  // the generic-proxy writes above, before the async-proxy read
-            asm volatile("bar.sync 1, %0;" ::"r"(32 * NUM_DECODE_WARPS) : "memory");  // every epilogue warp
-            if (warp == WARP_DEC0 && lane == 0 && !*abort) {
-                tma_store_2d(&tmap_d, m0, n0, sRed);
-                bulk_commit_group();
-                bulk_wait_group_read0();  // the source stays valid until the engine has read it
-            }
+            if (warp == WARP_DEC0 && lane == 0 && !*abort) bulk_wait_group_read0();  // sources valid until read
         }
     } else if (S == 1) {
         if (is_epi && have) {
@@ -707,7 +714,7 @@ static cudaError_t launch_sub(const GemmArgs &a, GemmParams p, int num_sms, cuda
         auto fn = get_encode_fn();
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.m), static_cast<cuuint64_t>(a.n)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.m) * 4};
-        const cuuint32_t box[2] = {static_cast<cuuint32_t>(PL::ROWS), static_cast<cuuint32_t>(BN)};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(PL::ROWS), 32u};
         const cuuint32_t estr[2] = {1, 1};
         p.dtma = fn && fn(&map_d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.dst, dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,

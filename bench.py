@@ -167,9 +167,10 @@ def _oracle_inputs():
     return ins
 
 
-def _oracle_sample(ins, entries_per_gemm, seed=0, threads=0):
+def _oracle_sample(ins, entries_per_gemm, seed=0, threads=0, keep=None):
     """Time the oracle on `entries_per_gemm` output entries of each GEMM
-    (threads = 0: the OpenMP default, all host cores)."""
+    (threads = 0: the OpenMP default, all host cores); with a list `keep`,
+    append (label, fmt, n indices, m indices, values, sum|W*X|) per GEMM."""
     import oracle
     rng = np.random.default_rng(seed)
     flops, t = 0.0, 0.0
@@ -177,10 +178,30 @@ def _oracle_sample(ins, entries_per_gemm, seed=0, threads=0):
         ni = rng.integers(0, N_TOKENS, entries_per_gemm)
         mj = rng.integers(0, m, entries_per_gemm)
         t0 = time.perf_counter()
-        oracle.matmul_entries(fmt, w, x, m, k, N_TOKENS, ni, mj, threads=threads)
+        ref, am = oracle.matmul_entries(fmt, w, x, m, k, N_TOKENS, ni, mj, threads=threads)
         t += time.perf_counter() - t0
         flops += 2.0 * k * entries_per_gemm
+        if keep is not None:
+            keep.append((label, fmt, ni, mj, ref, am))
     return flops, t
+
+
+def _check_timed_outputs(gemms, kept):
+    """The timed step's outputs (buffer copy 0, which every copy equals) at
+    the oracle's sampled entries, against the tensor-core tolerance
+    2e-3 * sum|W*X| + 1e-6."""
+    by = {(g["label"], g["fmt"]): g for g in gemms}
+    worst, bad, total = 0.0, 0, 0
+    for label, fmt, ni, mj, ref, am in kept:
+        got = by[(label, fmt)]["copies"][0]["dst"].cpu().numpy().astype(np.float64)[ni, mj]
+        ratio = np.abs(got - ref) / (2e-3 * am + 1e-6)
+        ratio[~np.isfinite(got)] = np.inf
+        worst = max(worst, float(ratio.max()))
+        bad += int((ratio > 1.0).sum())
+        total += ni.size
+    return {"entries": total, "outside_tolerance": bad, "worst_err_over_tol": round(worst, 4), "ok": bad == 0,
+            "what": "the timed step's outputs at the sampled entries against the f64 oracle, "
+                    "tolerance 2e-3*sum|W*X| + 1e-6"}
 
 
 def _oracle_calibrate(ins, budget_s, threads=0):
@@ -480,7 +501,8 @@ def run_ours(args):
         ins = _oracle_inputs()
         cores = _cores()  # before any one-thread run changes the OpenMP default
         entries = _oracle_calibrate(ins, 12.0, threads=cores)
-        f, t = _oracle_sample(ins, entries, seed=7, threads=cores)
+        kept = []
+        f, t = _oracle_sample(ins, entries, seed=7, threads=cores, keep=kept)
         entries1 = _oracle_calibrate(ins, 6.0, threads=1)
         f1, t1 = _oracle_sample(ins, entries1, seed=8, threads=1)
         cpu = {"value": f / t / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
@@ -488,7 +510,7 @@ def run_ours(args):
                "single_thread": {"value": f1 / t1 / 1e12, "unit": "TFLOP/s", "cores": 1,
                                  "sample": f"{entries1} random output entries of each of the 12 GEMMs "
                                            f"(f64 oracle, one thread, {t1:.1f} s)"},
-               "cpu": _cpu_model()}
+               "cpu": _cpu_model(), "check": _check_timed_outputs(gemms, kept)}
 
     q.qmm_destroy(h)
     if rank == 0:
@@ -622,7 +644,7 @@ def _moe_q8_sub(q, lib, h, torch, stream, tables, scales, x, in_f, n_ff, n_used,
 def run_sub_benches(q, lib, h, torch, synth, stream, hbm_gbs):
     sptr = stream.cuda_stream
     out = {"timing": f"median over {ROUNDS} rounds of back-to-back calls (weights rotated through more "
-                     "than 2x the L2 size)",
+                     "than 2x the L2 size); us_l2_warm: the same calls on one weight buffer, L2-resident",
            "gemv": [], "moe": None, "moe_q8": None, "moe_v2": None, "repack_v2": None, "moe_down": None,
            "moe_down_q8": None, "dequant": [], "fp4": None}
     # GEMV: rotate over enough weight copies to exceed L2 several times
@@ -639,12 +661,14 @@ def run_sub_benches(q, lib, h, torch, synth, stream, hbm_gbs):
                 calls = [(lambda wt=wt: lib.qmm_gemv(h, q.DTYPES[fmt], wt.data_ptr(), x.data_ptr(), d.data_ptr(),
                                                      m, k, n, sptr)) for wt in ws]
                 ms, lo, hi = _time_calls(torch, stream, calls, ncopy)
+                ms_warm, _, _ = _time_calls(torch, stream, calls[:1], ncopy)  # one weight buffer, L2-resident
                 tbytes = _alg_bytes(q, fmt, m, k, n)
                 wg, wf = _rate(wbytes, ms, hbm_gbs)
                 tg, tf = _rate(tbytes, ms, hbm_gbs)
                 out["gemv"].append({"dtype": fmt, "m": m, "k": k, "n": n, "us": round(ms * 1e3, 3),
                                     "us_min": round(lo * 1e3, 3), "us_max": round(hi * 1e3, 3),
-                                    "weight_gbs": wg, "frac_hbm": wf, "total_gbs": tg, "frac_hbm_total": tf})
+                                    "weight_gbs": wg, "frac_hbm": wf, "total_gbs": tg, "frac_hbm_total": tf,
+                                    "us_l2_warm": round(ms_warm * 1e3, 3)})
             del ws
     # MoE gate/up: 8 experts x {gate, up}, 4 rotated copies of the weight set
     in_f, n_ff, n_used = 4096, 2048, 8
@@ -669,9 +693,10 @@ def run_sub_benches(q, lib, h, torch, synth, stream, hbm_gbs):
     tbytes = wbytes + 4 * in_f + 2 * n_pairs * n_ff * 4 + 2 * n_pairs * (8 + 4)
     wg, wf = _rate(wbytes, ms, hbm_gbs)
     tg, tf = _rate(tbytes, ms, hbm_gbs)
+    ms_warm, _, _ = _time_calls(torch, stream, calls[:1], 40)  # one weight set (75.5 MB), L2-resident
     out["moe"] = {"us": round(ms * 1e3, 3), "us_min": round(lo * 1e3, 3), "us_max": round(hi * 1e3, 3),
                   "weight_bytes": wbytes, "weight_gbs": wg, "frac_hbm": wf, "total_bytes": tbytes,
-                  "total_gbs": tg, "frac_hbm_total": tf}
+                  "total_gbs": tg, "frac_hbm_total": tf, "us_l2_warm": round(ms_warm * 1e3, 3)}
     # the same products on int8 (Q8_1) activations: the quantizer and the
     # dp4a kernel, two launches per call, and the kernel alone
     try:

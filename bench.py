@@ -441,6 +441,40 @@ def run_ours(args):
                                f"x{TF32_OVER_F16:.3f} nominal ratio, HBM {hbm_gbs} GB/s; per GEMM the slower of "
                                "FLOPs at its tensor peak and algorithmic bytes at HBM"}
 
+    # ---- the same step replayed from a CUDA graph (one graph: a step on each
+    # buffer copy); reported beside the stream-issued headline ----
+    graph_step = None
+    if not args.no_graph:
+        try:
+            gstream = torch.cuda.Stream()
+            gstream.wait_stream(stream)
+            grun = _Runner(q, lib, h, torch, gstream, gemms, copies_n)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=gstream):
+                for c in range(copies_n):
+                    grun.step(c)
+            torch.cuda.synchronize()
+            reps = max(3, min(40, args.steps // copies_n))
+            gevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+            with torch.cuda.stream(gstream):
+                graph.replay()  # warm
+                for a, b in gevs:
+                    torch.cuda._sleep(1_500_000)
+                    a.record(gstream)
+                    graph.replay()
+                    b.record(gstream)
+            torch.cuda.synchronize()
+            if q.qmm_sync_status(h) != 0:
+                raise RuntimeError("device status set during the graph replays")
+            gms = _med([a.elapsed_time(b) / copies_n for a, b in gevs])
+            graph_step = {"ms_per_step": round(gms, 5), "tflops": round(flops_step / (gms * 1e-3) / 1e12, 2),
+                          "replays": reps, "steps_per_replay": copies_n,
+                          "what": "the 12 GEMMs of a step on each of the rotated buffer copies captured once, "
+                                  "replayed; median per step"}
+            del graph
+        except Exception as exc:  # reported, never fatal to the headline
+            graph_step = {"error": f"{type(exc).__name__}: {exc}"}
+
     # ---- the k-quant step (config 2): the same shapes with W in Q4_K / Q6_K ----
     kquant = None
     if not args.no_kquant:
@@ -548,7 +582,7 @@ def run_ours(args):
                                  f"{float(np.mean(step_ms)):.5f} ms",
                        "l2": f"inputs rotated over {copies_n} copies of {copy_mb:.0f} MB (L2 129 MB)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-            "per_dtype_tflops": per_dtype, "per_gemm": per_gemm, "kquant_step": kquant, "roofline": roofline,
+            "per_dtype_tflops": per_dtype, "per_gemm": per_gemm, "kquant_step": kquant, "graph_step": graph_step, "roofline": roofline,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
             "clocks": clk, "timed_wall_s": round(wall, 3), "sub": sub,
         }
@@ -1021,6 +1055,7 @@ def main(argv=None):
     ap.add_argument("--no-sub", action="store_true", help="skip the GEMV / MoE / dequant sub-benchmarks")
     ap.add_argument("--no-kquant", action="store_true", help="skip the Q4_K / Q6_K prefill step")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay of the step")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--only", default=None,
                     help="comma-separated shape labels to keep (profiling runs; not a headline workload)")

@@ -12,7 +12,8 @@
 //               box per stage over the rows viewed as 16-byte aligned row
 //               groups (G rows when G*row_bytes is a multiple of 16), else
 //               per-row 1-D bulk copies of 16-byte aligned supersets of each
-//               row;
+//               row; with f32 weights (tf32 MMA, no decode) the W tiles, so
+//               that two threads issue a stage's two 32 KB TMA requests;
 //   warp 1      TMEM allocation and the single MMA-issuing thread:
 //               tcgen05.mma.kind::f16, M=128, N=BN, K=16, sixteen per 256-wide
 //               k stage, A (decoded W) read from tensor memory, B (X) from
@@ -197,7 +198,7 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < MAXS; ++s) {
-            mbar_init(&ctl->b_full[s], 1);
+            mbar_init(&ctl->b_full[s], TF32 ? 2 : 1);  // f32 W: the W and X producers each arrive
             mbar_init(&ctl->b_empty[s], 1);
             mbar_init(&ctl->a_full[s], NUM_DECODE_WARPS);
             mbar_init(&ctl->a_empty[s], 1);
@@ -244,7 +245,35 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
     if (!p.w_early || warp == WARP_X) griddep_wait();
 
     if (warp == WARP_RAW) {
-        // ------------- raw weight producer (all 32 lanes) -------------
+        // ------------- raw weight producer (all 32 lanes); f32 W: the W tiles -------------
+        if constexpr (TF32) {
+            if (lane == 0) {
+                int last[BS];
+#pragma unroll
+                for (int s = 0; s < BS; ++s) last[s] = -1;
+                for (int i = 0; i < NK; ++i) {
+                    const int kt = kt0 + i, s = i % BS;
+                    const uint32_t ph = (i / BS) & 1;
+                    if (!mbar_wait_bounded(&ctl->b_empty[s], ph ^ 1, abort, p.status, p.limit_ns)) break;
+                    mbar_arrive_expect_tx(&ctl->b_full[s], PL::A_STAGE);
+                    if (p.x3d) {
+                        tma_load_3d(sA + s * PL::A_STAGE, &tmap_w, 0, m0, kt * PL::ATOMS, &ctl->b_full[s]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < PL::ATOMS; ++j) {
+                            const int kx = kt * KPS + j * (ATOM_ROW / PL::ELEM);
+                            tma_load_2d(sA + s * PL::A_STAGE + j * PL::A_ATOM, &tmap_w, kx, m0, &ctl->b_full[s]);
+                        }
+                    }
+                    last[s] = i;
+                }
+                if (*abort) {
+                    for (int s = 0; s < BS; ++s)
+                        if (last[s] >= 0) mbar_wait_drain(&ctl->b_full[s], (last[s] / BS) & 1, p.status, p.limit_ns);
+                }
+            }
+            __syncwarp();
+        }
         if constexpr (!TF32) {
             int last[RS];
 #pragma unroll
@@ -321,18 +350,15 @@ __global__ void __launch_bounds__(gemm::THREADS, 1)
                 const uint32_t ph = (i / BS) & 1;
                 if (!mbar_wait_bounded(&ctl->b_empty[s], ph ^ 1, abort, p.status, p.limit_ns)) break;
                 if (p.debug_skip && i == 0) continue;  // test hook: stage 0 never fills
-                mbar_arrive_expect_tx(&ctl->b_full[s], PL::B_STAGE + PL::A_STAGE);
+                mbar_arrive_expect_tx(&ctl->b_full[s], PL::B_STAGE);
                 if (p.x3d) {
                     // the whole stage (every 128-byte k atom of the tile rows) in one request:
                     // one SM's TMA engine spends about the same time per request up to 32 KB
-                    if constexpr (TF32) tma_load_3d(sA + s * PL::A_STAGE, &tmap_w, 0, m0, kt * PL::ATOMS, &ctl->b_full[s]);
                     tma_load_3d(sB + s * PL::B_STAGE, &tmap_x, 0, n0, kt * PL::ATOMS, &ctl->b_full[s]);
                 } else {
 #pragma unroll
                     for (int j = 0; j < PL::ATOMS; ++j) {
                         const int kx = kt * KPS + j * (ATOM_ROW / PL::ELEM);
-                        if constexpr (TF32)
-                            tma_load_2d(sA + s * PL::A_STAGE + j * PL::A_ATOM, &tmap_w, kx, m0, &ctl->b_full[s]);
                         tma_load_2d(sB + s * PL::B_STAGE + j * PL::B_ATOM, &tmap_x, kx, n0, &ctl->b_full[s]);
                     }
                 }

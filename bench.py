@@ -55,8 +55,8 @@ TF32_OVER_F16 = 1.1 / 2.25
 # bench reports null.
 GEMM_TRAFFIC_SOURCES = ("gemv_dequant_gemm_gb300/csrc/gemm_tc.cu", "gemv_dequant_gemm_gb300/csrc/decode.cuh",
                         "gemv_dequant_gemm_gb300/csrc/common.cuh")
-GEMM_TRAFFIC_SHA16 = "9476f3a329d5169d"
-GEMM_TRAFFIC_BYTES = 9.074e6
+GEMM_TRAFFIC_SHA16 = "173e19dc9c087f66"
+GEMM_TRAFFIC_BYTES = 9.075e6
 
 
 def _gemm_traffic():

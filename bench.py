@@ -501,17 +501,38 @@ def run_ours(args):
     # ---- e2e: host buffers through the public API ----
     e2e = None
     if not args.no_e2e:
-        pinned = []
+        # every input of a step (W and X of the 12 GEMMs) in one pinned host
+        # buffer, every result in another, each piece 256-byte aligned: one
+        # copy up and one copy down per step; the copies overlap the kernels
+        # of the neighbouring steps (inputs up on one stream, results down on
+        # another, kernels waiting for their step's inputs), and a device
+        # buffer set is refilled only after its last results are home
+        def _al(v):
+            return (v + 255) // 256 * 256
+        offs, pos = [], 0
         for g in gemms:
-            pinned.append({"w": torch.from_numpy(g["w_np"]).pin_memory(), "x": torch.from_numpy(g["x_np"]).pin_memory(),
-                           "dst": torch.empty(N_TOKENS, g["m"], dtype=torch.float32).pin_memory()})
-        h2d = sum(p["w"].numel() * p["w"].element_size() + p["x"].numel() * 4 for p in pinned)
-        d2h = sum(p["dst"].numel() * 4 for p in pinned)
+            ow = pos
+            pos = _al(pos + g["w_np"].nbytes)
+            ox = pos
+            pos = _al(pos + g["x_np"].nbytes)
+            offs.append((ow, ox))
+        in_bytes = pos
+        douts, pos = [], 0
+        for g in gemms:
+            douts.append(pos)
+            pos = _al(pos + N_TOKENS * g["m"] * 4)
+        out_bytes = pos
+        hin = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+        hout = torch.empty(out_bytes, dtype=torch.uint8).pin_memory()
+        for g, (ow, ox) in zip(gemms, offs):
+            hin[ow:ow + g["w_np"].nbytes].copy_(torch.from_numpy(g["w_np"].view(np.uint8).reshape(-1)))
+            hin[ox:ox + g["x_np"].nbytes].copy_(torch.from_numpy(g["x_np"].view(np.uint8).reshape(-1)))
+        din = [torch.empty(in_bytes, dtype=torch.uint8, device="cuda") for _ in range(copies_n)]
+        dout = [torch.empty(out_bytes, dtype=torch.uint8, device="cuda") for _ in range(copies_n)]
+        h2d = sum(g["w_np"].nbytes + g["x_np"].nbytes for g in gemms)
+        d2h = sum(N_TOKENS * g["m"] * 4 for g in gemms)
         e2e_steps = max(3, min(20, args.steps))
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        # copies overlap the kernels: each GEMM's inputs go up on one stream,
-        # its kernels wait only for them, its result comes down on another;
-        # a buffer set is refilled only after its previous result is home
         s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
         for rep in range(2):  # one untimed pass, then the timed one
             torch.cuda.synchronize()
@@ -521,24 +542,29 @@ def run_ours(args):
             home = {}
             for s in range(e2e_steps):
                 c = s % copies_n
-                for gi, (g, p) in enumerate(zip(gemms, pinned)):
-                    b = g["copies"][c]
-                    if (gi, c) in home:
-                        s_in.wait_event(home[(gi, c)])
-                    with torch.cuda.stream(s_in):
-                        b["w"].copy_(p["w"], non_blocking=True)
-                        b["x"].copy_(p["x"], non_blocking=True)
-                    up = torch.cuda.Event()
-                    up.record(s_in)
-                    stream.wait_event(up)
-                    run.launch(g, c)
-                    done = torch.cuda.Event()
-                    done.record(stream)
-                    s_out.wait_event(done)
-                    with torch.cuda.stream(s_out):
-                        p["dst"].copy_(b["dst"], non_blocking=True)
-                    home[(gi, c)] = torch.cuda.Event()
-                    home[(gi, c)].record(s_out)
+                if c in home:
+                    s_in.wait_event(home[c])
+                with torch.cuda.stream(s_in):
+                    din[c].copy_(hin, non_blocking=True)
+                up = torch.cuda.Event()
+                up.record(s_in)
+                stream.wait_event(up)
+                base_in, base_out = din[c].data_ptr(), dout[c].data_ptr()
+                for gi, g in enumerate(gemms):
+                    ow, ox = offs[gi]
+                    ws = g["copies"][c]["ws"]
+                    st = lib.qmm_gemm(h, q.DTYPES[g["fmt"]], base_in + ow, base_in + ox, base_out + douts[gi],
+                                      g["m"], g["k"], N_TOKENS, ws.data_ptr() if g["wsb"] else None, g["wsb"],
+                                      stream.cuda_stream)
+                    if st:
+                        raise q.QmmError(st, "qmm_gemm")
+                done = torch.cuda.Event()
+                done.record(stream)
+                s_out.wait_event(done)
+                with torch.cuda.stream(s_out):
+                    hout.copy_(dout[c], non_blocking=True)
+                home[c] = torch.cuda.Event()
+                home[c].record(s_out)
             for ev in home.values():
                 stream.wait_event(ev)
             ev1.record(stream)
@@ -546,8 +572,9 @@ def run_ours(args):
         e2e_ms = slowest_rank_ms(ev0.elapsed_time(ev1) / e2e_steps, world, "cuda")
         e2e = {"value": round(job_tflops(world, flops_step, e2e_ms), 3), "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 4),
-               "overlap": "inputs copied up on one stream and results down on another, kernels on the compute "
-                          "stream waiting for their own inputs; every copy of every step inside the timed region"}
+               "overlap": "each step's inputs packed in one pinned buffer and copied up in one copy on one "
+                          "stream, its results down in one copy on another, kernels on the compute stream; "
+                          "every copy of every step inside the timed region"}
 
     # ---- a6-a8, f1-f3: GEMV, MoE, dequant (GB/s vs HBM) ----
     sub = None if args.no_sub else run_sub_benches(q, lib, h, torch, synth, stream, hbm_gbs)

@@ -201,8 +201,9 @@ __global__ void __launch_bounds__(gs::MAX_THREADS) gemv_sk_kernel(const gs::Para
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = p.splits;
     const int z = blockIdx.y;  // rank in the cluster (cluster dims 1 x S x 1, grid y = S)
-    const int row0 = blockIdx.x * p.rbk;
-    const int rows = min(p.rbk, p.m - row0);
+    // rows spread evenly over the grid (at most p.rbk per CTA)
+    const int row0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * p.m / gridDim.x);
+    const int rows = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * p.m / gridDim.x) - row0;
     const int64_t kb0 = static_cast<int64_t>(z) * p.us * UW;  // first k of the slice
     const int64_t sbo = kb0 / QK * BB;                         // its byte offset in a row
     const uintptr_t wbase = reinterpret_cast<uintptr_t>(p.w);
@@ -504,8 +505,17 @@ template <int F, int NV, int J> cudaError_t launch_sk_j(gs::Params p, SkPlan pl,
     cudaError_t e = cudaFuncSetAttribute(gemv_sk_kernel<F, NV, J>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    const dim3 grid(static_cast<unsigned>((p.m + pl.rbk - 1) / pl.rbk), static_cast<unsigned>(pl.splits),
-                    static_cast<unsigned>(nz));
+    // a grid that gives every SM the same number of CTAs when one wave still
+    // holds it (rows then spread evenly, at most rbk per CTA)
+    int64_t gx = (p.m + pl.rbk - 1) / pl.rbk;
+    {
+        const int occ = resident(pl.tk, smem);
+        const int64_t per = static_cast<int64_t>(pl.splits) * nz;
+        int64_t g2 = gx;
+        while ((g2 * per) % num_sms != 0) ++g2;
+        if (g2 <= p.m && g2 * per <= static_cast<int64_t>(occ) * num_sms) gx = g2;
+    }
+    const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(pl.splits), static_cast<unsigned>(nz));
     return launch_pdl(gemv_sk_kernel<F, NV, J>, grid, dim3(pl.tk), smem, st, dim3(1, pl.splits, 1), p);
 }
 

@@ -10,7 +10,9 @@
 // enough resident warps to hide it, and keeps the per-weight instruction
 // count low.
 //
-//   * A CTA owns RB consecutive rows and one k-slice of them (split S of a
+//   * A CTA owns up to RB consecutive rows (the rows spread evenly over a
+//     grid of whole waves per SM when one wave holds it) and one k-slice of
+//     them (split S of a
 //     cluster of S CTAs along k; S = 1, whole rows, unless that leaves too
 //     few warps to cover the SMs).  n > 4 (or n > 2 when that avoids a k
 //     split) spreads the activation rows over several CTAs.  Thread 0 moves the rows' slice bytes into

@@ -12,10 +12,10 @@
 //
 //   * A CTA owns up to RB consecutive rows (the rows spread evenly over a
 //     grid of whole waves per SM when one wave holds it) and one k-slice of
-//     them (split S of a
-//     cluster of S CTAs along k; S = 1, whole rows, unless that leaves too
-//     few warps to cover the SMs).  n > 4 (or n > 2 when that avoids a k
-//     split) spreads the activation rows over several CTAs.  Thread 0 moves the rows' slice bytes into
+//     them: a split S of a cluster of S CTAs along k, S = 1 (whole rows)
+//     unless that leaves too few warps to cover the SMs.  n > 4 (or n > 2
+//     when that avoids a k split) spreads the activation rows over several
+//     CTAs.  Thread 0 moves the rows' slice bytes into
 //     shared memory with bulk copies (one copy when the slice is the whole
 //     row, one per row otherwise; 16-byte aligned supersets, any row stride)
 //     after warming L2 with them before the dependency wait.

@@ -351,6 +351,11 @@ __global__ void __launch_bounds__(gv::THREADS, gemv_ctas_per_sm<NV>()) gemv_kern
 // i in lane i, and writes them to a per-warp partial buffer.  The producer
 // warp, when the stage's slot comes back to it, adds the partials of a
 // team's warps in warp order and stores the results.
+// Grouped mode (the MoE down projection): a stage holds the same rows of
+// all `group` pair matrices of one token, one slice per matrix, and team u
+// takes every row of pair u's slice with that pair's activation row in its
+// registers; the producer then sums the pairs of each row in pair order into
+// dst [tokens][rows], so no workspace and no second kernel are needed.
 // ---------------------------------------------------------------------------
 namespace gr {
 constexpr int COMPUTE_WARPS = 16;
@@ -372,6 +377,8 @@ struct Params {
     int rows_per_mat, mats, n_pairs, n_used, tokens;
     int tk, J, rt, teams, stage_rows;
     int stages_per_mat, total_stages, stage_bytes, ring;
+    int group;      // grouped mode: pairs per token (0: off); stages then walk (token, row block)
+    int sub_bytes;  // grouped mode: bytes of one matrix's slice of a stage
     uint32_t *status;
     uint64_t limit_ns;
 };
@@ -485,6 +492,28 @@ struct StageWalk {
     }
 };
 
+// Grouped mode, one row: the 16 warps' partials (team u = warps u*WPT ..),
+// each team's summed in warp order and scaled by sc[u], the teams added in
+// order.  All loads first (compile-time indices), then the arithmetic.
+template <int WPT> __device__ __forceinline__ float group_row_sum(const float *pb, int o, const float *sc) {
+    constexpr int W = gr::COMPUTE_WARPS, G = W / WPT;
+    float v[W], s[G];
+#pragma unroll
+    for (int i = 0; i < W; ++i) v[i] = pb[i * gr::PART + o];
+#pragma unroll
+    for (int u = 0; u < G; ++u) s[u] = sc[u];
+    float a = 0.0f;
+#pragma unroll
+    for (int u = 0; u < G; ++u) {
+        float sum = 0.0f;
+#pragma unroll
+        for (int w = 0; w < WPT; ++w) sum += v[u * WPT + w];
+        const float t = s[u] * sum;
+        a = u == 0 ? t : a + t;
+    }
+    return a;
+}
+
 template <int F, int NV, int JM>
 __global__ void __launch_bounds__(gr::THREADS, 1) gemv_rx_kernel(const gr::Params p) {
     using namespace gr;
@@ -545,24 +574,72 @@ __global__ void __launch_bounds__(gr::THREADS, 1) gemv_rx_kernel(const gr::Param
                     const int r0 = sw.sp * p.stage_rows;
                     const int rows = min(p.stage_rows, p.rows_per_mat - r0);
                     const bool bad = ctl->bad[slot] != 0;
-                    const float scale = !moe ? 1.0f : (table ? ctl->mscale[mat] : __ldg(p.scales + mat));
                     const float *pb = partial + slot * COMPUTE_WARPS * PART;
-                    for (int o = lane; o < rows * NV; o += 32) {
-                        const int rl = o / NV, v = o % NV;
-                        const int tm = rl / p.rt, i = rl % p.rt;
-                        float sum = 0.0f;
-                        for (int w = 0; w < wpt; ++w) sum += pb[(tm * wpt + w) * PART + i * NVP + v];
-                        const float val = bad ? nan : scale * sum;
-                        if (moe)
-                            p.dst[static_cast<int64_t>(mat) * p.rows_per_mat + r0 + rl] = val;
-                        else
-                            p.dst[static_cast<int64_t>(v) * p.rows_per_mat + r0 + rl] = val;
+                    if (p.group) {
+                        // token `mat`: each pair's row sum scaled, then the pairs
+                        // added in pair order (NV == 1)
+                        const float *sc = table ? ctl->mscale + mat * p.group : p.scales + mat * p.group;
+                        for (int o = lane; o < rows; o += 32) {
+                            float a;
+                            switch (wpt) {
+                            case 1: a = group_row_sum<1>(pb, o, sc); break;
+                            case 2: a = group_row_sum<2>(pb, o, sc); break;
+                            case 4: a = group_row_sum<4>(pb, o, sc); break;
+                            case 8: a = group_row_sum<8>(pb, o, sc); break;
+                            default: a = group_row_sum<16>(pb, o, sc); break;
+                            }
+                            p.dst[static_cast<int64_t>(mat) * p.rows_per_mat + r0 + o] = bad ? nan : a;
+                        }
+                    } else {
+                        const float scale = !moe ? 1.0f : (table ? ctl->mscale[mat] : __ldg(p.scales + mat));
+                        for (int o = lane; o < rows * NV; o += 32) {
+                            const int rl = o / NV, v = o % NV;
+                            const int tm = rl / p.rt, i = rl % p.rt;
+                            float sum = 0.0f;
+                            for (int w = 0; w < wpt; ++w) sum += pb[(tm * wpt + w) * PART + i * NVP + v];
+                            const float val = bad ? nan : scale * sum;
+                            if (moe)
+                                p.dst[static_cast<int64_t>(mat) * p.rows_per_mat + r0 + rl] = val;
+                            else
+                                p.dst[static_cast<int64_t>(v) * p.rows_per_mat + r0 + rl] = val;
+                        }
                     }
                     if (bad && lane == 0) atomicOr(p.status, kDevBadPtr);
                 }
                 sw.next(p.stages_per_mat, p.ring);
             }
-            if (j < nst && lane == 0) {
+            if (j < nst && lane == 0 && p.group) {
+                // grouped: the stage's rows of each of token `mat`'s pair
+                // matrices, one bulk copy per matrix into its slice
+                const int mat = ld.mat;
+                const int r0 = ld.sp * p.stage_rows;
+                const int rows = min(p.stage_rows, p.rows_per_mat - r0);
+                bool ok = true;
+                uint32_t tx = 0;
+                for (int u = 0; u < p.group; ++u) {
+                    const int pr = mat * p.group + u;
+                    const uint8_t *mp = table ? ctl->mptr[pr] : static_cast<const uint8_t *>(p.w_ptrs[pr]);
+                    if (mp == nullptr || (reinterpret_cast<uintptr_t>(mp) & 15u) != 0) ok = false;
+                    const uintptr_t src = reinterpret_cast<uintptr_t>(mp) + static_cast<uintptr_t>(r0) * p.rb;
+                    tx += ((static_cast<uint32_t>(src & 15u) + static_cast<uint32_t>(rows * p.rb)) + 15u) & ~15u;
+                }
+                ctl->bad[slot] = ok ? 0 : 1;
+                if (!ok) {
+                    mbar_arrive(&ctl->full[slot]);
+                } else {
+                    mbar_arrive_expect_tx(&ctl->full[slot], tx);
+                    for (int u = 0; u < p.group; ++u) {
+                        const int pr = mat * p.group + u;
+                        const uint8_t *mp = table ? ctl->mptr[pr] : static_cast<const uint8_t *>(p.w_ptrs[pr]);
+                        const uint8_t *src = mp + static_cast<int64_t>(r0) * p.rb;
+                        const uintptr_t a = reinterpret_cast<uintptr_t>(src) & ~uintptr_t(15);
+                        const uint32_t len = (static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src) - a) +
+                                              static_cast<uint32_t>(rows * p.rb) + 15u) & ~15u;
+                        bulk_load_1d(ring + slot * p.stage_bytes + u * p.sub_bytes, reinterpret_cast<const void *>(a),
+                                     len, &ctl->full[slot]);
+                    }
+                }
+            } else if (j < nst && lane == 0) {
                 const int mat = ld.mat;
                 const int r0 = ld.sp * p.stage_rows;
                 const int rows = min(p.stage_rows, p.rows_per_mat - r0);
@@ -620,9 +697,9 @@ __global__ void __launch_bounds__(gr::THREADS, 1) gemv_rx_kernel(const gr::Param
         for (int j = 0; j < nst; ++j, wk.next(p.stages_per_mat, p.ring)) {
             const int slot = wk.slot;
             const int mat = wk.mat;
-            if (mat != cur_mat) {  // uniform over the CTA: the stage decides it
+            if (mat != cur_mat) {  // uniform over the CTA (the team's, grouped): the stage decides it
                 cur_mat = mat;
-                tok = moe ? (mat % p.n_pairs) / p.n_used : 0;
+                tok = p.group ? mat * p.group + team : (moe ? (mat % p.n_pairs) / p.n_used : 0);
             }
             if (tok != cur_tok) {
                 cur_tok = tok;
@@ -650,8 +727,10 @@ __global__ void __launch_bounds__(gr::THREADS, 1) gemv_rx_kernel(const gr::Param
             const int r0 = wk.sp * p.stage_rows;
             const int rows = min(p.stage_rows, p.rows_per_mat - r0);
             const bool bad = !dead && ctl->bad[slot] != 0;
-            const uint8_t *mp = !moe ? p.w : (table ? ctl->mptr[mat] : static_cast<const uint8_t *>(p.w_ptrs[mat]));
-            const uint8_t *buf = ring + slot * p.stage_bytes +
+            // grouped: the team's pair is activation row `tok`, its slice the team's
+            const int wm = p.group ? tok : mat;
+            const uint8_t *mp = !moe ? p.w : (table ? ctl->mptr[wm] : static_cast<const uint8_t *>(p.w_ptrs[wm]));
+            const uint8_t *buf = ring + slot * p.stage_bytes + (p.group ? team * p.sub_bytes : 0) +
                                  ((reinterpret_cast<uintptr_t>(mp) + static_cast<int64_t>(r0) * p.rb) & 15u);
             float *pw = partial + (slot * COMPUTE_WARPS + warp) * PART;
             const uint32_t sbase = smem_u32(buf);
@@ -665,7 +744,7 @@ __global__ void __launch_bounds__(gr::THREADS, 1) gemv_rx_kernel(const gr::Param
                 if (!bad && !dead) {
 #pragma unroll
                     for (int r = 0; r < RG; ++r) {
-                        const int rl = team * p.rt + i0 + r;
+                        const int rl = (p.group ? 0 : team * p.rt) + i0 + r;
                         const uint8_t *rowp = buf + static_cast<int64_t>(rl) * p.rb;
                         const uint32_t rbase = sbase + static_cast<uint32_t>(rl) * static_cast<uint32_t>(p.rb);
 #pragma unroll
@@ -817,6 +896,61 @@ template <int F, int NV> static cudaError_t launch_rx(const gr::Params &p, int n
     }
 }
 
+// Grouped register-X plan for the MoE down projection: the `group` pairs of
+// a token are the teams (team size 512/group threads, covering k exactly
+// with J <= JM units each), and every team takes all rows of a stage: about
+// 40 KB of weights per stage in whole groups of four rows, at most PART (one
+// partial per row and warp), fewer while that leaves SMs without a stage.
+template <int F> static bool plan_rx_group(gr::Params &p, int group, int tokens, int num_sms) {
+    using namespace gr;
+    constexpr int UW = Unit<F>::W;
+    constexpr int JM = jmax<F, 1>();
+    if (UW > XREG || p.k < 2048 || p.k % UW != 0 || group < 2 || NT % group != 0) return false;
+    const int tk = NT / group;
+    if (tk % 32 != 0) return false;
+    const int64_t nunits = p.k / UW;
+    if (nunits % tk != 0 || nunits / tk > JM) return false;
+    p.tk = tk;
+    p.J = static_cast<int>(nunits / tk);
+    p.teams = group;
+    p.group = group;
+    int64_t r = 40960 / (static_cast<int64_t>(group) * std::max<int64_t>(p.rb, 1));
+    r = std::max<int64_t>(4, std::min<int64_t>(r, PART)) / 4 * 4;
+    while (r > 4 && static_cast<int64_t>(tokens) * ((p.rows_per_mat + r - 1) / r) < num_sms) r -= 4;
+    p.rt = static_cast<int>(r);
+    p.stage_rows = p.rt;
+    p.stages_per_mat = (p.rows_per_mat + p.stage_rows - 1) / p.stage_rows;
+    p.total_stages = p.stages_per_mat * tokens;
+    // a slice holds its rows plus the source's offset from 16 bytes
+    p.sub_bytes = static_cast<int>((static_cast<int64_t>(p.stage_rows) * p.rb + 15 + 15) / 16 * 16);
+    p.stage_bytes = group * p.sub_bytes;
+    const int fixed = static_cast<int>(sizeof(Ctl)) + 1024;
+    const int per_stage = p.stage_bytes + COMPUTE_WARPS * PART * 4;
+    p.ring = std::min(MAX_RING, (SMEM_BUDGET - fixed) / per_stage);
+    return p.ring >= 2;
+}
+
+template <int F>
+static cudaError_t launch_group_f(gr::Params rp, int group, int tokens, int num_sms, cudaStream_t st, bool *used) {
+    *used = plan_rx_group<F>(rp, group, tokens, num_sms);
+    return *used ? launch_rx<F, 1>(rp, num_sms, st) : cudaSuccess;
+}
+
+// The grouped down projection when its plan exists (*used), else nothing.
+static cudaError_t launch_group_any(int dtype, const gr::Params &rp, int group, int tokens, int num_sms,
+                                    cudaStream_t st, bool *used) {
+    switch (dtype) {
+    case QMM_F32: return launch_group_f<QMM_F32>(rp, group, tokens, num_sms, st, used);
+    case QMM_Q4_0: return launch_group_f<QMM_Q4_0>(rp, group, tokens, num_sms, st, used);
+    case QMM_Q8_0: return launch_group_f<QMM_Q8_0>(rp, group, tokens, num_sms, st, used);
+    case QMM_Q4_K: return launch_group_f<QMM_Q4_K>(rp, group, tokens, num_sms, st, used);
+    case QMM_Q6_K: return launch_group_f<QMM_Q6_K>(rp, group, tokens, num_sms, st, used);
+    case QMM_NVFP4: return launch_group_f<QMM_NVFP4>(rp, group, tokens, num_sms, st, used);
+    case QMM_NVFP4_V2: return launch_group_f<QMM_NVFP4_V2>(rp, group, tokens, num_sms, st, used);
+    default: *used = false; return cudaErrorInvalidValue;
+    }
+}
+
 // Register-X kernel when its plan exists, else the shared-memory X kernel.
 template <int F, int NV>
 static cudaError_t launch_any(gr::Params rp, const gv::Params &gp, int num_sms, cudaStream_t st) {
@@ -957,8 +1091,10 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const float *__restric
 cudaError_t launch_moe_down(int dtype, const void *const *w_ptrs, int64_t rb, const float *scales, const float *h,
                             float *y, float *part, int64_t n_ff, int64_t gin, int n_used, int tokens, int num_sms,
                             uint32_t *status, uint64_t limit_ns, cudaStream_t st) {
-    // the pair products: the MoE GEMV with one matrix per pair, each pair its
-    // own activation row (n_used = 1 makes the activation row the pair index)
+    // the grouped register-X kernel when it has a plan; else the pair
+    // products -- the MoE GEMV with one matrix per pair, each pair its own
+    // activation row (n_used = 1 makes the activation row the pair index) --
+    // then the combine kernel
     const int n_pairs = n_used * tokens;
     gv::Params p = {};
     p.w_ptrs = w_ptrs;
@@ -974,6 +1110,14 @@ cudaError_t launch_moe_down(int dtype, const void *const *w_ptrs, int64_t rb, co
     p.tokens = n_pairs;
     p.status = status;
     p.limit_ns = limit_ns;
+    if (n_used > 1) {
+        // grouped: each token's pairs in one stage, summed by the kernel into y
+        gr::Params rp = rx_params(p);
+        rp.dst = y;
+        bool used = false;
+        const cudaError_t eg = launch_group_any(dtype, rp, n_used, tokens, num_sms, st, &used);
+        if (used || eg != cudaSuccess) return eg;
+    }
     plan_stages(p, static_cast<int64_t>(n_pairs) * n_ff * 4, gv::SMEM_BUDGET / 2);
     cudaError_t e = dispatch_any(dtype, rx_params(p), p, 1, num_sms, st);
     if (e != cudaSuccess || n_used == 1) return e;

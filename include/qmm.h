@@ -197,8 +197,15 @@ int qmm_moe_gemv(qmm_handle h, qmm_dtype t, const void *const *w_ptrs, const flo
  *     overwritten (not accumulated into).
  *   - workspace: device scratch of qmm_moe_down_workspace_bytes(gin, n_used,
  *     t_tokens) bytes (0 when n_used == 1: then pass NULL), 16-byte aligned,
- *     overlapping no other argument; it holds the per-pair products, which a
- *     second kernel sums per token in the order u = 0, 1, ... so results are
+ *     overlapping no other argument, any contents.  When n_ff >= 2048 and
+ *     n_used divides 512 so that
+ *     teams of 512/n_used threads cover n_ff in whole blocks (16 weights
+ *     for NVFP4, 8 otherwise) with at most 32 values per thread -- at
+ *     n_ff = 2048: n_used 4 or 8 for NVFP4, 2, 4 or 8 for the others -- one
+ *     kernel takes each token's pairs together and sums them itself,
+ *     leaving the workspace unused; otherwise the workspace holds the
+ *     per-pair products and a second kernel sums them.  Either way each
+ *     token's pairs are added in the order u = 0, 1, ... so results are
  *     deterministic.
  * Any dtype; fp32 decode and FMA; accuracy |y - exact| <= 1e-5 *
  * sum_u |scales[j]| * sum_c |W_j * hact_j|.  Sizes: 1 <= n_used, t_tokens;

@@ -155,3 +155,54 @@ def test_moe_down_argument_errors(h):
                        yb, wsb)
     assert e.value.status == 9
     assert np.all(np.isnan(y.cpu().numpy()))  # nothing was launched
+
+
+# ---- the grouped register-X kernel (rows of 2048, 4 or 8 pairs per token):
+# a stage holds the same rows of all of a token's pair matrices and the
+# kernel sums the pairs itself, with no workspace round trip ----------------
+
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_moe_down_grouped_every_format(h, fmt):
+    n_ff, gin, n_used, t = 2048, 261, 4, 2  # 261 rows: a partial last stage
+    n_pairs = n_used * t
+    mats = [weights(fmt, gin, n_ff, seed=synth.nvfp4_matrix_seed(8, j, 2)) for j in range(n_pairs)]
+    scales = _scales(n_pairs)
+    hact = synth.activations(n_pairs, n_ff, seed=H_SEED + 2)
+    st, y = _run_down(h, fmt, mats, scales, hact, n_ff, gin, n_used, t)
+    assert st == 0
+    ref, am = oracle.moe_down(fmt, mats, scales, hact, n_ff, gin, n_used, t)
+    assert_close(y, ref, am, FMA_REL, what=f"grouped {fmt}")
+
+
+def test_moe_down_grouped_device_table(h):
+    # 8 pairs x 40 tokens = 320 pairs: pointers and scales come from the
+    # device table, not the kernel's shared-memory copy of the first 256
+    n_ff, gin, n_used, t = 2048, 24, 8, 40
+    n_pairs = n_used * t
+    mats = [synth.nvfp4_rows(synth.nvfp4_matrix_seed(9, j, 2), gin, n_ff) for j in range(n_pairs)]
+    scales = _scales(n_pairs)
+    hact = synth.activations(n_pairs, n_ff, seed=H_SEED + 3)
+    st, y = _run_down(h, "nvfp4", mats, scales, hact, n_ff, gin, n_used, t)
+    assert st == 0
+    ref, am = oracle.moe_down("nvfp4", mats, scales, hact, n_ff, gin, n_used, t)
+    assert_close(y, ref, am, FMA_REL, what="grouped, device table")
+
+
+def test_moe_down_grouped_bad_table_entry_is_reported(h):
+    # pair 5 (token 1) misaligned: token 1's rows NaN, token 0 exact
+    n_ff, gin, n_used, t = 2048, 40, 4, 2
+    n_pairs = n_used * t
+    mats = [weights("nvfp4", gin, n_ff, seed=synth.nvfp4_matrix_seed(10, j, 2)) for j in range(n_pairs)]
+    scales = _scales(n_pairs)
+    hact = synth.activations(n_pairs, n_ff, seed=H_SEED)
+
+    def fix(p):
+        p[5] += 4
+        return p
+
+    st, y = _run_down(h, "nvfp4", mats, scales, hact, n_ff, gin, n_used, t, ptr_fix=fix)
+    assert st == 4
+    assert np.all(np.isnan(y[1]))
+    ref, am = oracle.moe_down("nvfp4", mats, scales, hact, n_ff, gin, n_used, t)
+    assert_close(y[0], ref[0], am[0], FMA_REL, what="token 0")
+    assert q.qmm_sync_status(h) == 0

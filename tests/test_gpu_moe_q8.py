@@ -320,3 +320,58 @@ def test_q8_fused_argument_errors(h):
         q.qmm_moe_down_q8_fused(h, "nvfp4", table, scales, 0, yd, in_f, 40, 1, 1)
     assert e.value.status == 1  # no activation
     assert np.all(np.isnan(y.cpu().numpy())) and np.all(np.isnan(yd.cpu().numpy()))
+
+
+# ---- more down-projection shapes: 2 to 16 pairs per token, ragged row
+# counts, the longest rows, both layouts ------------------------------------
+
+@pytest.mark.parametrize("fmt,n_ff,gin,n_used,t", [("nvfp4", 2048, 261, 2, 3), ("nvfp4_v2", 1024, 261, 4, 2),
+                                                    ("nvfp4", 128, 37, 16, 2), ("nvfp4_v2", 8192, 19, 8, 1)])
+def test_moe_down_q8_pair_counts(h, fmt, n_ff, gin, n_used, t):
+    n_pairs = n_used * t
+    mats = _as_fmt(fmt, [synth.nvfp4_rows(synth.nvfp4_matrix_seed(11, j, 2), gin, n_ff) for j in range(n_pairs)],
+                   gin, n_ff)
+    scales = _scales(n_pairs)
+    hact = synth.activations(n_pairs, n_ff, seed=H_SEED + 4)
+    qd, dd = _quantize(h, hact, n_pairs, n_ff)
+    st, y = _run_down(h, fmt, mats, scales, qd, dd, n_ff, gin, n_used, t)
+    assert st == 0
+    qo, do = oracle.quantize_q8_1(hact, n_pairs, n_ff)
+    ref, am = oracle.moe_down_q8(fmt, mats, scales, qo, do, n_ff, gin, n_used, t)
+    assert_close(y, ref, am, FMA_REL, what=f"down q8 {fmt} n_used={n_used}")
+    # the fused call (quantizing inside the kernel) writes the same bits
+    _, table = _table(mats)
+    y1 = nan_filled(t, gin)
+    wsb = q.qmm_moe_down_workspace_bytes(gin, n_used, t)
+    ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda")
+    q.qmm_moe_down_q8_fused(h, fmt, table, dev(scales), dev(hact), y1, n_ff, gin, n_used, t, ws, wsb)
+    assert q.qmm_sync_status(h) == 0
+    assert np.array_equal(y1.cpu().numpy().view(np.uint32), y.view(np.uint32))
+
+
+def test_moe_down_q8_device_table_and_bad_entry(h):
+    # 8 pairs x 70 tokens = 560 pairs: pointers and scales from the device
+    # table (the kernel copies up to 512); pair 13 (token 1) misaligned:
+    # token 1's rows NaN, the other tokens exact
+    n_ff, gin, n_used, t = 128, 16, 8, 70
+    n_pairs = n_used * t
+    mats = [synth.nvfp4_rows(synth.nvfp4_matrix_seed(12, j, 2), gin, n_ff) for j in range(n_pairs)]
+    scales = _scales(n_pairs)
+    hact = synth.activations(n_pairs, n_ff, seed=H_SEED + 5)
+    qd, dd = _quantize(h, hact, n_pairs, n_ff)
+    dm, table = _table(mats)
+    ptrs = [a.data_ptr() for a in dm]
+    ptrs[13] += 4
+    table = torch.tensor(ptrs, dtype=torch.int64, device="cuda")
+    y = nan_filled(t, gin)
+    wsb = q.qmm_moe_down_workspace_bytes(gin, n_used, t)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    q.qmm_moe_down_q8(h, "nvfp4", table, dev(scales), qd, dd, y, n_ff, gin, n_used, t, ws, wsb)
+    assert q.qmm_sync_status(h) == 4
+    y = y.cpu().numpy()
+    assert np.all(np.isnan(y[1]))
+    qo, do = oracle.quantize_q8_1(hact, n_pairs, n_ff)
+    ref, am = oracle.moe_down_q8("nvfp4", mats, scales, qo, do, n_ff, gin, n_used, t)
+    keep = [i for i in range(t) if i != 1]
+    assert_close(y[keep], ref[keep], am[keep], FMA_REL, what="down q8, other tokens")
+    assert q.qmm_sync_status(h) == 0

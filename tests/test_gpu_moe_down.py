@@ -161,9 +161,10 @@ def test_moe_down_argument_errors(h):
 # a stage holds the same rows of all of a token's pair matrices and the
 # kernel sums the pairs itself, with no workspace round trip ----------------
 
-@pytest.mark.parametrize("fmt", FORMATS)
-def test_moe_down_grouped_every_format(h, fmt):
-    n_ff, gin, n_used, t = 2048, 261, 4, 2  # 261 rows: a partial last stage
+@pytest.mark.parametrize("fmt,n_used", [(f, 4) for f in FORMATS] + [("q8_0", 2), ("f32", 8), ("nvfp4", 8)])
+def test_moe_down_grouped_every_format(h, fmt, n_used):
+    # teams of 128 threads (4 pairs), 256 (2 pairs: 8-weight blocks only) and 64 (8 pairs)
+    n_ff, gin, t = 2048, 261, 2  # 261 rows: a partial last stage
     n_pairs = n_used * t
     mats = [weights(fmt, gin, n_ff, seed=synth.nvfp4_matrix_seed(8, j, 2)) for j in range(n_pairs)]
     scales = _scales(n_pairs)
@@ -171,7 +172,7 @@ def test_moe_down_grouped_every_format(h, fmt):
     st, y = _run_down(h, fmt, mats, scales, hact, n_ff, gin, n_used, t)
     assert st == 0
     ref, am = oracle.moe_down(fmt, mats, scales, hact, n_ff, gin, n_used, t)
-    assert_close(y, ref, am, FMA_REL, what=f"grouped {fmt}")
+    assert_close(y, ref, am, FMA_REL, what=f"grouped {fmt} n_used={n_used}")
 
 
 def test_moe_down_grouped_device_table(h):

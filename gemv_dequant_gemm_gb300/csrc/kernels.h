@@ -28,9 +28,11 @@ cudaError_t launch_moe_gemv(int dtype, const void *const *w_ptrs, int64_t rb, co
                             float *y, int64_t in_f, int64_t n_ff, int n_used, int n_pairs, int tokens, int num_sms,
                             uint32_t *status, uint64_t limit_ns, cudaStream_t st);
 
-// MoE down projection: per-pair products of gin rows over n_ff into part
-// [n_pairs][gin] (into y directly when n_used == 1), then y[t][gin] = the
-// fixed-order sum of each token's n_used pairs.
+// MoE down projection: y[t][gin] = the fixed-order sum (u = 0, 1, ...) of
+// token t's n_used pair products of gin rows over n_ff -- in one grouped
+// register-X launch when a token's pairs fit its k teams (part unused),
+// else per-pair products into part [n_pairs][gin] (into y directly when
+// n_used == 1) and the combine kernel.
 cudaError_t launch_moe_down(int dtype, const void *const *w_ptrs, int64_t rb, const float *scales, const float *h,
                             float *y, float *part, int64_t n_ff, int64_t gin, int n_used, int tokens, int num_sms,
                             uint32_t *status, uint64_t limit_ns, cudaStream_t st);

@@ -2,8 +2,9 @@
 // step of the v1 prefill path in aprender-serve 0.70.2 cublas_prefill/mod.rs,
 // module doc).
 //
-// One thread decodes 8 consecutive weights and writes them as two 16-byte
-// stores; the grid strides over the m*k/8 groups.  The file also holds the
+// One thread decodes 8 consecutive weights into a shared buffer; each CTA's
+// chunk of 256 groups leaves in one bulk store; the grid strides over the
+// chunks.  The file also holds the
 // repack of NVFP4 rows into the V2 layout (a byte permutation).  Bit-exact: every value is
 // the format's value rounded once to float32 (decode.cuh).
 #include "kernels.h"
@@ -11,6 +12,46 @@
 #include "l2hint.cuh"
 
 namespace qmm {
+
+// 1-D bulk store shared -> global (the TMA engine), tracked by the issuing
+// thread's bulk groups; both addresses 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void dq_bulk_store(void *gdst, const void *smem_src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(gdst)),
+                 "r"(smem_u32(smem_src)), "r"(bytes)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Chunks of 256 consecutive 8-weight groups (8 KB of output, contiguous:
+// group g's values are out[8g .. 8g+7]): thread t decodes group t of the
+// chunk into a shared buffer, and one bulk store writes the chunk, so the
+// fp32 stream leaves through the TMA engine instead of 512 per-thread
+// stores.  Two buffers: a chunk's buffer is reused two chunks later, once
+// its store has read it.
+template <typename Idx, typename Decode>
+__device__ __forceinline__ void dequant_chunks(float *__restrict__ out, Idx total, Decode decode) {
+    __shared__ __align__(128) float4 buf[2][2 * 256];
+    const Idx nchunks = (total + 255) / 256;
+    int b = 0;
+    for (Idx c = blockIdx.x; c < nchunks; c += gridDim.x, b ^= 1) {
+        if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        __syncthreads();
+        const Idx g = c * 256 + threadIdx.x;
+        if (g < total) {
+            float v[8];
+            decode(g, v);
+            buf[b][2 * threadIdx.x] = make_float4(v[0], v[1], v[2], v[3]);
+            buf[b][2 * threadIdx.x + 1] = make_float4(v[4], v[5], v[6], v[7]);
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const Idx n = total - c * 256 < 256 ? total - c * 256 : 256;
+            dq_bulk_store(out + c * 256 * 8, &buf[b][0], static_cast<uint32_t>(n) * 32u);
+        }
+    }
+    if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
 
 template <int F, typename Idx>
 __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict__ w, float *__restrict__ out,
@@ -29,18 +70,11 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict_
     griddep_wait();
     griddep_launch();
     const Idx gpr = k / 8;  // groups per row
-    const Idx total = m * gpr;
-    for (Idx g = static_cast<Idx>(blockIdx.x) * blockDim.x + threadIdx.x; g < total;
-         g += static_cast<Idx>(gridDim.x) * blockDim.x) {
+    dequant_chunks(out, m * gpr, [&](Idx g, float (&v)[8]) {
         const Idx r = g / gpr;
         const Idx e0 = (g - r * gpr) * 8;
-        const uint8_t *blk = w + r * rb + (e0 / QK) * BB;
-        float v[8];
-        Dec8<F, LdG>::run(blk, static_cast<int>(e0 % QK), ts, v);
-        float4 *o = reinterpret_cast<float4 *>(out + r * k + e0);
-        o[0] = make_float4(v[0], v[1], v[2], v[3]);
-        o[1] = make_float4(v[4], v[5], v[6], v[7]);
-    }
+        Dec8<F, LdG>::run(w + r * rb + (e0 / QK) * BB, static_cast<int>(e0 % QK), ts, v);
+    });
 }
 
 // f32 weights: the decoded value is the weight itself.
@@ -75,21 +109,15 @@ __global__ void __launch_bounds__(256) dequant_nvfp4_v2_kernel(const uint8_t *__
     griddep_wait();
     griddep_launch();
     const int64_t gpr = k / 8;
-    const int64_t total = m * gpr;
-    for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < total;
-         g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    dequant_chunks(out, m * gpr, [&](int64_t g, float (&v)[8]) {
         const int64_t r = g / gpr;
         const int64_t e0 = (g - r * gpr) * 8;
         const uint8_t *row = w + r * rb;
         const uint32_t codes = __ldg(reinterpret_cast<const unsigned int *>(row + e0 / 2));
         const float s = e4m3_to_f32(__ldg(row + k / 2 + e0 / 16));
-        float v[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(__fmul_rn(e2m1_to_f32((codes >> (4 * j)) & 15u), s), ts);
-        float4 *o = reinterpret_cast<float4 *>(out + r * k + e0);
-        o[0] = make_float4(v[0], v[1], v[2], v[3]);
-        o[1] = make_float4(v[4], v[5], v[6], v[7]);
-    }
+    });
 }
 
 // NVFP4 36-byte groups -> V2 rows: one thread moves one group (nine 4-byte

@@ -15,10 +15,13 @@ namespace qmm {
 
 // 1-D bulk store shared -> global (the TMA engine), tracked by the issuing
 // thread's bulk groups; both addresses 16-byte aligned, bytes % 16 == 0.
-__device__ __forceinline__ void dq_bulk_store(void *gdst, const void *smem_src, uint32_t bytes) {
+__device__ __forceinline__ void dq_bulk_store_nocommit(void *gdst, const void *smem_src, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(gdst)),
                  "r"(smem_u32(smem_src)), "r"(bytes)
                  : "memory");
+}
+__device__ __forceinline__ void dq_bulk_store(void *gdst, const void *smem_src, uint32_t bytes) {
+    dq_bulk_store_nocommit(gdst, smem_src, bytes);
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
@@ -140,11 +143,58 @@ __global__ void __launch_bounds__(256) nvfp4_repack_v2_kernel(const uint8_t *__r
     }
 }
 
+// The same repack for k % 256 == 0 (rows of a multiple of 16 bytes, groups
+// per row a multiple of 4): chunks of 256 consecutive groups, thread t
+// loading group t and placing its code words and scale word into shared
+// buffers laid out as the V2 row segments; then thread j writes the chunk's
+// part of row j of the chunk with two bulk stores (codes, scales), all
+// 16-byte aligned because every segment starts and ends on a group index
+// that is a multiple of 4.  Two buffer pairs; a pair is reused once the
+// stores that read it (each by the thread that issued them) are done.
+__global__ void __launch_bounds__(256) nvfp4_repack_v2_chunks_kernel(const uint8_t *__restrict__ v1,
+                                                                     uint8_t *__restrict__ v2, int64_t m,
+                                                                     int64_t k) {
+    __shared__ __align__(128) uint4 cbuf[2][2 * 256];  // code words, 32 bytes per group
+    __shared__ __align__(128) unsigned int sbuf[2][256];  // scale words
+    griddep_wait();
+    griddep_launch();
+    const int64_t gpr = k / 64, rb = gpr * 36, total = m * gpr;
+    const int64_t nchunks = (total + 255) / 256;
+    int b = 0;
+    for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x, b ^= 1) {
+        asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        __syncthreads();
+        const int64_t g0 = c * 256, g1 = g0 + 256 < total ? g0 + 256 : total;
+        const int64_t g = g0 + threadIdx.x;
+        if (g < g1) {  // rows are contiguous: group g starts at 36 g
+            const unsigned int *src = reinterpret_cast<const unsigned int *>(v1 + g * 36);
+            sbuf[b][threadIdx.x] = __ldg(src);
+            cbuf[b][2 * threadIdx.x] = make_uint4(__ldg(src + 1), __ldg(src + 2), __ldg(src + 3), __ldg(src + 4));
+            cbuf[b][2 * threadIdx.x + 1] = make_uint4(__ldg(src + 5), __ldg(src + 6), __ldg(src + 7), __ldg(src + 8));
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        const int64_t r = g0 / gpr + threadIdx.x;  // this thread's row of the chunk
+        if (r * gpr < g1) {
+            const int64_t qlo = r * gpr < g0 ? g0 - r * gpr : 0;
+            const int64_t qhi = (r + 1) * gpr < g1 ? gpr : g1 - r * gpr;
+            const int64_t o = r * gpr + qlo - g0;  // the segment's first group within the chunk
+            uint8_t *row = v2 + r * rb;
+            dq_bulk_store_nocommit(row + qlo * 32, &cbuf[b][2 * o], static_cast<uint32_t>((qhi - qlo) * 32));
+            dq_bulk_store_nocommit(row + k / 2 + qlo * 4, &sbuf[b][o], static_cast<uint32_t>((qhi - qlo) * 4));
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+    }
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 cudaError_t launch_nvfp4_repack_v2(const uint8_t *v1, uint8_t *v2, int64_t m, int64_t k, int num_sms,
                                    cudaStream_t st) {
     const int64_t total = m * (k / 64);
     const int64_t want = (total + 255) / 256;
     const int grid = static_cast<int>(want < 8LL * num_sms ? want : 8LL * num_sms);
+    if (k % 256 == 0 && (reinterpret_cast<uintptr_t>(v2) & 15u) == 0)
+        return launch_pdl(nvfp4_repack_v2_chunks_kernel, dim3(grid), dim3(256), 0, st, dim3(1, 1, 1), v1, v2, m, k);
     return launch_pdl(nvfp4_repack_v2_kernel, dim3(grid), dim3(256), 0, st, dim3(1, 1, 1), v1, v2, m, k);
 }
 

@@ -19,7 +19,11 @@ def _v1_v2(m, k, seed):
     return v1, oracle.nvfp4_repack_v2(v1, m, k)
 
 
-@pytest.mark.parametrize("m,k", [(1, 64), (37, 320), (2048, 4096)])
+# k % 256 == 0 takes the chunked kernel (bulk stores of each chunk's row
+# segments): 4 groups a row (64 rows a chunk), 20 a row (rows straddling
+# chunks), a last chunk of a few groups; the others take the per-thread kernel
+@pytest.mark.parametrize("m,k", [(1, 64), (37, 320), (2048, 4096), (5, 256), (53, 256), (37, 1280), (3, 2304),
+                                 (1000, 2048)])
 def test_repack_matches_the_oracle(h, m, k):
     v1, want = _v1_v2(m, k, 0x7001 + m)
     out = torch.full((want.size,), 0xA5, dtype=torch.uint8, device="cuda")

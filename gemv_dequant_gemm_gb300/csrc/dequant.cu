@@ -3,7 +3,7 @@
 // module doc).
 //
 // One thread decodes 8 consecutive weights into a shared buffer; each CTA's
-// chunk of 256 groups leaves in one bulk store; the grid strides over the
+// chunk of 128 groups leaves in one bulk store; the grid strides over the
 // chunks.  The file also holds the
 // repack of NVFP4 rows into the V2 layout (a byte permutation).  Bit-exact: every value is
 // the format's value rounded once to float32 (decode.cuh).
@@ -25,21 +25,23 @@ __device__ __forceinline__ void dq_bulk_store(void *gdst, const void *smem_src, 
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
-// Chunks of 256 consecutive 8-weight groups (8 KB of output, contiguous:
-// group g's values are out[8g .. 8g+7]): thread t decodes group t of the
-// chunk into a shared buffer, and one bulk store writes the chunk, so the
-// fp32 stream leaves through the TMA engine instead of 512 per-thread
-// stores.  Two buffers: a chunk's buffer is reused two chunks later, once
-// its store has read it.
+// Chunks of 128 consecutive 8-weight groups (4 KB of output, contiguous:
+// group g's values are out[8g .. 8g+7]) for CTAs of 128 threads: thread t
+// decodes group t of the chunk into a shared buffer, and one bulk store
+// writes the chunk, so the fp32 stream leaves through the TMA engine instead
+// of 256 per-thread stores.  Two buffers: a chunk's buffer is reused two
+// chunks later, once its store has read it.  (Chunks of 256 groups for
+// 256-thread CTAs ran 2-3 % slower.)
 template <typename Idx, typename Decode>
 __device__ __forceinline__ void dequant_chunks(float *__restrict__ out, Idx total, Decode decode) {
-    __shared__ __align__(128) float4 buf[2][2 * 256];
-    const Idx nchunks = (total + 255) / 256;
+    constexpr int T = 128;
+    __shared__ __align__(128) float4 buf[2][2 * T];
+    const Idx nchunks = (total + T - 1) / T;
     int b = 0;
     for (Idx c = blockIdx.x; c < nchunks; c += gridDim.x, b ^= 1) {
         if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
         __syncthreads();
-        const Idx g = c * 256 + threadIdx.x;
+        const Idx g = c * T + threadIdx.x;
         if (g < total) {
             float v[8];
             decode(g, v);
@@ -49,15 +51,15 @@ __device__ __forceinline__ void dequant_chunks(float *__restrict__ out, Idx tota
         fence_proxy_async_smem();
         __syncthreads();
         if (threadIdx.x == 0) {
-            const Idx n = total - c * 256 < 256 ? total - c * 256 : 256;
-            dq_bulk_store(out + c * 256 * 8, &buf[b][0], static_cast<uint32_t>(n) * 32u);
+            const Idx n = total - c * T < T ? total - c * T : T;
+            dq_bulk_store(out + c * T * 8, &buf[b][0], static_cast<uint32_t>(n) * 32u);
         }
     }
     if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 template <int F, typename Idx>
-__global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict__ w, float *__restrict__ out,
+__global__ void __launch_bounds__(128) dequant_kernel(const uint8_t *__restrict__ w, float *__restrict__ out,
                                                       Idx m, Idx k, Idx rb, float ts) {
     constexpr int QK = Fmt<F>::QK, BB = Fmt<F>::BB;
     // an equal slice of the packed weights into L2 per CTA, before waiting
@@ -97,7 +99,7 @@ __global__ void __launch_bounds__(256) copy_f32_kernel(const float *__restrict__
 // so every row starts on a 4-byte boundary): one thread decodes 8
 // consecutive weights from one code word and one scale byte, each value
 // (e2m1 * e4m3, exact) times ts rounded once, as for the 36-byte groups.
-__global__ void __launch_bounds__(256) dequant_nvfp4_v2_kernel(const uint8_t *__restrict__ w,
+__global__ void __launch_bounds__(128) dequant_nvfp4_v2_kernel(const uint8_t *__restrict__ w,
                                                                float *__restrict__ out, int64_t m, int64_t k,
                                                                float ts) {
     const int64_t rb = k / 32 * 18;
@@ -202,12 +204,12 @@ template <int F>
 static cudaError_t launch_dequant_t(const void *w, float *out, int64_t m, int64_t k, int64_t rb, float ts,
                                     int num_sms, cudaStream_t st) {
     const int64_t total = m * (k / 8);
-    const int64_t want = (total + 255) / 256;
-    const int grid = static_cast<int>(want < 8LL * num_sms ? want : 8LL * num_sms);
+    const int64_t want = (total + 127) / 128;
+    const int grid = static_cast<int>(want < 16LL * num_sms ? want : 16LL * num_sms);
     if (total < (1LL << 31) && m * k < (1LL << 31))
-        return launch_pdl(dequant_kernel<F, uint32_t>, dim3(grid), dim3(256), 0, st, dim3(1, 1, 1), static_cast<const uint8_t *>(w),
+        return launch_pdl(dequant_kernel<F, uint32_t>, dim3(grid), dim3(128), 0, st, dim3(1, 1, 1), static_cast<const uint8_t *>(w),
                           out, static_cast<uint32_t>(m), static_cast<uint32_t>(k), static_cast<uint32_t>(rb), ts);
-    return launch_pdl(dequant_kernel<F, int64_t>, dim3(grid), dim3(256), 0, st, dim3(1, 1, 1), static_cast<const uint8_t *>(w), out,
+    return launch_pdl(dequant_kernel<F, int64_t>, dim3(grid), dim3(128), 0, st, dim3(1, 1, 1), static_cast<const uint8_t *>(w), out,
                       m, k, rb, ts);
 }
 
@@ -226,9 +228,9 @@ cudaError_t launch_dequant(int dtype, const void *w, float *out, int64_t m, int6
     case QMM_Q6_K: return launch_dequant_t<QMM_Q6_K>(w, out, m, k, rb, ts, num_sms, st);
     case QMM_NVFP4: return launch_dequant_t<QMM_NVFP4>(w, out, m, k, rb, ts, num_sms, st);
     case QMM_NVFP4_V2: {
-        const int64_t want = (m * (k / 8) + 255) / 256;
-        const int grid = static_cast<int>(want < 8LL * num_sms ? want : 8LL * num_sms);
-        return launch_pdl(dequant_nvfp4_v2_kernel, dim3(grid), dim3(256), 0, st, dim3(1, 1, 1),
+        const int64_t want = (m * (k / 8) + 127) / 128;
+        const int grid = static_cast<int>(want < 16LL * num_sms ? want : 16LL * num_sms);
+        return launch_pdl(dequant_nvfp4_v2_kernel, dim3(grid), dim3(128), 0, st, dim3(1, 1, 1),
                           static_cast<const uint8_t *>(w), out, m, k, ts);
     }
     default: return cudaErrorInvalidValue;
